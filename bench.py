@@ -1,0 +1,461 @@
+#!/usr/bin/env python3
+"""Benchmark of the lookahead sparse KV staging + sparse decode attention path on GB300.
+
+Metric: sparse-decode tok/s at Qwen3-8B attention shapes (36 layers, 32 query / 8 KV heads,
+head_dim 128, bf16), batch 128, 16K context, block 16, 2048-token budget, fetch cap 0.05, with
+the HBM and host-link roofline fractions of the kernels that carry it.
+
+One step = one decode step of the whole hot path over all 36 layers: per layer, sparse
+attention of the step's query over the resident slot pool, then staging from the draft query
+(block scoring against the min/max summaries, per-head top-K, capped diff/evict, host->HBM
+gather of the admitted blocks), the staging overlapped with the later layers' attention.
+`value` = batch * steps / device time of the timed steps (inputs resident in HBM);
+`e2e` = the same through the C ABI with the step's queries and drafts copied from pinned host
+memory and the step's attention outputs copied back, inside the timed region.
+
+Full KV lives in page-locked host memory. The 288 GiB of the full batch do not fit the host,
+so requests alias `--alias` distinct host buffers (request r reads buffer r mod alias); every
+request still has its own summaries, selections, slot pool and queries, so device work and
+host-link traffic per step are those of the full batch.
+
+`--impl reference` times the CPU oracle (binary64 C, all host cores) on a bounded sample of
+the same workload per step: one layer of the full batch, extrapolated to a full step.
+Multi-GPU (torchrun): each rank runs its own replica of the workload (requests shard with no
+data exchange), timing is the max over ranks, `value` sums all ranks' tokens.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse-decode tok/s, Qwen3-8B attn 16K b128; % of HBM & host-link roofline"
+WORKLOAD = "qwen3_8b_16k_b128"
+
+
+def log(*a):
+    print("[bench]", *a, file=sys.stderr, flush=True)
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=64)
+    p.add_argument("--warmup", type=int, default=4)
+    p.add_argument("--impl", choices=["okv", "reference"], default="okv")
+    p.add_argument("--alias", type=int, default=16, help="distinct host KV buffers the batch aliases")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--threads", type=int, default=0)
+    return p.parse_args()
+
+
+# ---- distributed plumbing (replicas: barrier and max-over-ranks only) -------------------------
+
+class Dist:
+    def __init__(self, want_gpu: bool):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch
+            import torch.distributed as dist
+            backend = "nccl" if want_gpu and torch.cuda.is_available() else "gloo"
+            if backend == "nccl":
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+            self.backend = backend
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        dev = "cuda" if self.backend == "nccl" else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ---- measurement helpers ---------------------------------------------------------------------
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="okv_clocks_", suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def pinned_h2d_gbs(nbytes=1 << 30, reps=5) -> float:
+    import torch
+    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    h.fill_(1)
+    for _ in range(2):
+        d.copy_(h, non_blocking=True)
+    torch.cuda.synchronize()
+    best = 1e30
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        d.copy_(h, non_blocking=True)
+        b.record()
+        b.synchronize()
+        best = min(best, a.elapsed_time(b))
+    del h, d
+    return nbytes / (best / 1e3) / 1e9
+
+
+# ---- workload setup ----------------------------------------------------------------------------
+
+class Workload:
+    def __init__(self, alias: int, threads: int):
+        import numpy as np
+        import synth
+        self.np = np
+        self.synth = synth
+        self.w = synth.WORKLOADS[WORKLOAD]
+        w = self.w
+        self.B, self.L, self.Hq, self.Hkv, self.d = w.batch, w.layers, w.q_heads, w.kv_heads, w.head_dim
+        self.n_tok = w.context
+        self.nb = -(-w.context // w.block_size)
+        self.kb = w.budget_tokens // w.block_size
+        self.alias = max(1, min(alias, self.B))
+        self.ids = np.arange(self.B, dtype=np.int32)
+        self.keys = (self.ids % self.alias).astype(np.int32)
+        self.threads = threads or os.cpu_count() or 1
+
+    def config(self):
+        from sparse_kv_cache_draft_gb300 import BF16, Config
+        w = self.w
+        return Config(w.layers, w.q_heads, w.kv_heads, w.head_dim, w.block_size, w.budget_tokens, w.batch,
+                      self.nb, w.fetch_cap, BF16)
+
+    def host_kv(self):
+        from sparse_kv_cache_draft_gb300 import HostBuffer
+        cfg = self.config()
+        t0 = time.time()
+        bufs = [HostBuffer(cfg.host_bytes(self.nb)) for _ in range(self.alias)]
+        t1 = time.time()
+        for k, b in enumerate(bufs):
+            self.synth.fill_kv(b.ptr, self.w, k, 0, self.n_tok, self.nb, n_threads=self.threads)
+        log(f"host KV: {self.alias} x {cfg.host_bytes(self.nb) / 2**30:.2f} GiB pinned in {t1 - t0:.1f}s, "
+            f"generated in {time.time() - t1:.1f}s")
+        return bufs
+
+    def queries(self, layer, step, kind, out=None):
+        return self.synth.queries(self.w, layer, step, kind, self.ids, self.keys, out=out, n_threads=self.threads)
+
+    def config_json(self):
+        w = self.w
+        return {"workload": WORKLOAD, "model_shapes": "Qwen3-8B attention", "batch": self.B, "seq_len": self.n_tok,
+                "layers": self.L, "q_heads": self.Hq, "kv_heads": self.Hkv, "head_dim": self.d,
+                "block_size": w.block_size, "budget_tokens": w.budget_tokens, "fetch_cap": w.fetch_cap,
+                "host_kv_buffers": self.alias, "parallelism": "replicas",
+                "l2": "no flush: per-step working set (54 GiB of summaries and slot pool) >> 129 MB L2"}
+
+
+# ---- CPU oracle timing (cpu_baseline leg and the reference arm) -------------------------------
+
+class OracleTimer:
+    """The oracle as it stands, on the host cores, over one layer of the full batch per sample."""
+
+    def __init__(self, wl: Workload, bufs, layers):
+        import oracle
+        self.oracle = oracle
+        self.wl = wl
+        w = wl.w
+        self.layers = list(layers)
+        self.model = oracle.OracleModel(layers=w.layers, q_heads=w.q_heads, kv_heads=w.kv_heads,
+                                        head_dim=w.head_dim, block_size=w.block_size,
+                                        budget_tokens=w.budget_tokens, dtype=w.dtype,
+                                        req_ptrs=[bufs[int(k)].ptr for k in wl.keys], cap_blocks=[wl.nb] * wl.B,
+                                        n_tok=wl.n_tok, n_threads=wl.threads, layers_kept=self.layers)
+        self.C = oracle.fetch_cap_blocks(w.fetch_cap, wl.kb)
+        self.ready = set()
+
+    def prepare(self, layer):
+        if layer in self.ready:
+            return
+        self.model.build_summaries(layer)
+        self.model.stage(layer, self.wl.queries(layer, -1, 1), self.oracle.fetch_cap_blocks(1.0, self.wl.kb), 0)
+        self.ready.add(layer)
+
+    def sample(self, layer, step):
+        """Seconds for one layer's attend + stage of decode step `step` over the full batch."""
+        self.prepare(layer)
+        q = self.wl.queries(layer, step, 0)
+        dr = self.wl.queries(layer, step, 1)
+        t0 = time.perf_counter()
+        self.model.attend(layer, q)
+        self.model.stage(layer, dr, self.C, step + 1)
+        return time.perf_counter() - t0
+
+
+def cpu_baseline(wl: Workload, bufs, n_layers=2):
+    t = OracleTimer(wl, bufs, range(n_layers))
+    secs = [t.sample(l, 0) for l in range(n_layers)]
+    per_step = statistics.mean(secs) * wl.L
+    return {"value": wl.B / per_step, "unit": "tok/s", "cores": wl.threads, "kind": "oracle",
+            "sample": f"decode step 0 (attend + stage) of layers 0..{n_layers - 1} for all {wl.B} requests x "
+                      f"{wl.Hkv} KV heads, {sum(secs):.1f}s wall on {wl.threads} threads; tok/s = batch / "
+                      f"(mean layer time x {wl.L} layers), extrapolated"}
+
+
+# ---- the okv arm -------------------------------------------------------------------------------
+
+def run_okv(args, dist: Dist):
+    import numpy as np
+    import torch
+    from sparse_kv_cache_draft_gb300 import Context, HostBuffer, load_library
+
+    load_library()
+    torch.cuda.set_device(dist.local)
+    wl = Workload(args.alias, args.threads)
+    cfg = wl.config()
+    B, L, Hq, d = wl.B, wl.L, wl.Hq, wl.d
+    K, W = args.steps, args.warmup
+    bufs = wl.host_kv()
+    t0 = time.time()
+    ctx = Context(cfg)
+    for r in range(B):
+        ctx.add_request(r, bufs[int(wl.keys[r])].ptr, wl.nb, wl.n_tok)
+    log(f"context + {B} requests registered in {time.time() - t0:.1f}s")
+
+    # inputs for the bootstrap, W warm-up and K timed steps (pinned host copies for e2e)
+    n_steps = W + K
+    qshape = (L, B, Hq, d)
+    per_step = L * B * Hq * d
+    t0 = time.time()
+    q_host = HostBuffer(n_steps * per_step * 2)
+    d_host = HostBuffer((n_steps + 1) * per_step * 2)
+    qh = q_host.numpy(np.uint16, (n_steps,) + qshape)
+    dh = d_host.numpy(np.uint16, (n_steps + 1,) + qshape)  # dh[t + 1] = draft of step t
+    for t in range(-1, n_steps):
+        for l in range(L):
+            if t >= 0:
+                wl.queries(l, t, 0, out=qh[t, l])
+            wl.queries(l, t, 1, out=dh[t + 1, l])
+    log(f"inputs for {n_steps} steps generated in {time.time() - t0:.1f}s")
+
+    def as_bf16(a):
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+
+    q_dev = as_bf16(qh).to("cuda")
+    d_dev = as_bf16(dh).to("cuda")
+    out = torch.empty(qshape, dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    # bootstrap staging from the draft of step -1 at fetch cap 1.0 (fills the empty pools)
+    for l in range(L):
+        ctx.stage(l, d_dev[0, l], 0, 1.0)
+    for t in range(W):
+        ctx.step(q_dev[t], d_dev[t + 1], out, t + 1)
+    torch.cuda.synchronize()
+    ctx.sync()
+
+    # timed region: K decode steps, inputs resident in HBM
+    ctx.set_timing(True)
+    torch.cuda.synchronize()
+    dist.barrier()
+    sampler = ClockSampler(dist.local)
+    sampler.start()
+    time.sleep(0.3)
+    launches0 = ctx.launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for t in range(W, W + K):
+        ctx.step(q_dev[t], d_dev[t + 1], out, t + 1)
+    ctx.join(stream)
+    ev1.record(stream)
+    ev1.synchronize()
+    clocks = sampler.stop()
+    launches = ctx.launch_count() - launches0
+    ms = ev0.elapsed_time(ev1)
+    timing = ctx.read_timing()
+    ctx.set_timing(False)
+    assert ctx.sync(60_000) == 0
+    dist.barrier()
+    ms_max = dist.max(ms)
+
+    # e2e: the same steps through the C ABI from pinned host inputs, outputs copied back
+    out_host = HostBuffer(per_step * 2)
+    oh = as_bf16(out_host.numpy(np.uint16, qshape))
+    q_in = torch.empty(qshape, dtype=torch.bfloat16, device="cuda")
+    d_in = torch.empty(qshape, dtype=torch.bfloat16, device="cuda")
+    qh_t, dh_t = as_bf16(qh), as_bf16(dh)
+    torch.cuda.synchronize()
+    dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i, t in enumerate(range(W, W + K)):
+        q_in.copy_(qh_t[t], non_blocking=True)
+        d_in.copy_(dh_t[t + 1], non_blocking=True)
+        ctx.step(q_in, d_in, out, W + K + i + 1)
+        oh.copy_(out, non_blocking=True)
+    ctx.join(stream)
+    e1.record(stream)
+    e1.synchronize()
+    e2e_ms = dist.max(e0.elapsed_time(e1))
+    assert ctx.sync(60_000) == 0
+
+    # rooflines
+    hbm_peak, peak_src = measured_peaks()
+    h2d_peak = pinned_h2d_gbs()
+    slot_bytes = cfg.block_size * 2 * d * 2
+    n_att_calls = L * K
+    att_ms = timing["ms"]["attend"] / n_att_calls
+    att_bytes = (timing["attended_slots"] / n_att_calls) * slot_bytes + 2 * B * Hq * d * 2 + B * wl.Hkv * wl.kb * 4
+    att_gbs = att_bytes / (att_ms / 1e3) / 1e9
+    sc_ms = timing["ms"]["score_topk"] / n_att_calls
+    sc_bytes = B * wl.Hkv * wl.nb * 2 * d * 2 + B * Hq * d * 2
+    sc_gbs = sc_bytes / (sc_ms / 1e3) / 1e9
+    gather_bytes = timing["fetched_blocks"] * slot_bytes
+    gather_ms = timing["ms"]["gather"]
+    gather_gbs = gather_bytes / (gather_ms / 1e3) / 1e9 if gather_ms > 0 else 0.0
+    step_ms = ms_max / K
+    hbm_step_bytes = L * (att_bytes + sc_bytes)
+
+    value = dist.world * B * K / (ms_max / 1e3)
+    e2e_value = dist.world * B * K / (e2e_ms / 1e3)
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tok/s", "n_gpus": dist.world, "steps": K,
+        "warmup": W, "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": wl.config_json(),
+        "clocks": clocks,
+        "e2e": {"value": round(e2e_value, 1), "unit": "tok/s", "h2d_bytes_per_step": 2 * per_step * 2,
+                "d2h_bytes_per_step": per_step * 2},
+        "gpu_launches": int(launches),
+        "roofline": {"bound": "hbm", "kernel": "sparse GQA decode attention (okv_attend)",
+                     "achieved": round(att_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(att_gbs / hbm_peak, 4), "traffic": None,
+                     "peak_source": f"hbm_gbs, {peak_src}",
+                     "bytes_per_launch": int(att_bytes), "ms_per_launch": round(att_ms, 5)},
+        "scoring_roofline": {"bound": "hbm", "kernel": "block scoring + top-K", "achieved": round(sc_gbs, 1),
+                             "peak": hbm_peak, "unit": "GB/s", "frac": round(sc_gbs / hbm_peak, 4),
+                             "bytes_per_launch": int(sc_bytes), "ms_per_launch": round(sc_ms, 5)},
+        "host_link": {"kernel": "host->HBM block gather", "achieved": round(gather_gbs, 1),
+                      "peak": round(h2d_peak, 1), "unit": "GB/s", "frac": round(gather_gbs / h2d_peak, 4),
+                      "peak_source": "pinned cudaMemcpy H2D of 1 GiB measured in this run",
+                      "bytes_per_step": int(gather_bytes / K)},
+        "step_hbm": {"bytes_per_step": int(hbm_step_bytes),
+                     "achieved_gbs": round(hbm_step_bytes / (step_ms / 1e3) / 1e9, 1),
+                     "frac": round(hbm_step_bytes / (step_ms / 1e3) / 1e9 / hbm_peak, 4)},
+        "kernel_ms_per_step": {k: round(v / K, 4) for k, v in timing["ms"].items() if v > 0},
+        "attention_ms_per_layer": round(att_ms, 5),
+    }
+    if not args.no_cpu_baseline and dist.rank == 0:
+        t0 = time.time()
+        res["cpu_baseline"] = cpu_baseline(wl, bufs)
+        log(f"cpu baseline sample took {time.time() - t0:.1f}s")
+    ctx.close()
+    for b in bufs:
+        b.free()
+    return res
+
+
+def run_reference(args, dist: Dist):
+    if dist.rank != 0:
+        return None
+    wl = Workload(args.alias, args.threads)
+    bufs = wl.host_kv()
+    n_layers_used = 4
+    t = OracleTimer(wl, bufs, range(n_layers_used))
+    for l in range(n_layers_used):
+        t.prepare(l)
+    for s in range(args.warmup):
+        t.sample(s % n_layers_used, s)
+    secs = [t.sample(s % n_layers_used, s) for s in range(args.warmup, args.warmup + args.steps)]
+    per_step = statistics.mean(secs) * wl.L
+    value = wl.B / per_step
+    sample = (f"per step: attend + stage of one layer (rotating over layers 0..{n_layers_used - 1}) for all {wl.B} "
+              f"requests x {wl.Hkv} KV heads; step time = layer time x {wl.L} layers (extrapolated)")
+    for b in bufs:
+        b.free()
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tok/s", "n_gpus": dist.world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_step * 1e3, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": wl.config_json(),
+            "cpu_baseline": {"value": round(value, 3), "unit": "tok/s", "cores": wl.threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse_args()
+    dist = Dist(want_gpu=args.impl == "okv")
+    try:
+        res = run_okv(args, dist) if args.impl == "okv" else run_reference(args, dist)
+        if res is not None and dist.rank == 0:
+            print(json.dumps(res), flush=True)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,191 @@
+/*
+ * okv: lookahead sparse KV staging and sparse decode attention on one GB300 (sm_103a).
+ *
+ * The operations follow OasisKV ("OasisKV: Scaling In-Decode KV Cache Beyond HBM with
+ * Lookahead Sparse Prefetching", arXiv 2608.08097; summary page paperlayer.ai/abs/2608.08097v1):
+ * the full KV cache stays off-GPU in host memory, HBM holds per-block key summaries and a
+ * sparse working set of blocks, and a draft (lookahead) query stages the next step's blocks
+ * ("4 System Design"). One library context serves one model on one GPU.
+ *
+ * Conventions
+ *  - Every call returns an okv_status and never throws across the ABI. On failure,
+ *    okv_last_error(ctx) holds a one-line reason.
+ *  - "unit" = one (layer, request, kv head). "Kb" = budget_tokens / block_size slots per unit.
+ *  - Device pointers are caller-owned device memory (e.g. torch tensors), contiguous, of the
+ *    context's storage dtype unless stated. They must stay valid until the work enqueued on
+ *    the given stream has finished.
+ *  - `stream` arguments are cudaStream_t handles passed as void* (NULL = legacy default stream).
+ *  - Calls are asynchronous unless their name starts with okv_read_ or is okv_sync.
+ *  - A context is used from one host thread at a time.
+ *  - Kernels never trap: an invalid index found on the device is recorded in a device error
+ *    word and the access is skipped; okv_sync and the okv_read_* calls report it as
+ *    OKV_EDEVICE.
+ *
+ * Host KV layout of one request (caller-owned, page-locked, e.g. from okv_host_alloc):
+ *   [layers][kv_heads][capacity_blocks][2][block_size][head_dim], index 0 of the "2" axis is K,
+ *   1 is V, storage dtype. One block of one unit (K and V of block_size tokens) is contiguous.
+ */
+#ifndef OKV_H
+#define OKV_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define OKV_API __attribute__((visibility("default")))
+#else
+#define OKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  OKV_OK = 0,
+  OKV_EINVAL = 1,   /* bad argument or unsupported shape */
+  OKV_ENOMEM = 2,   /* device or page-locked host allocation failed */
+  OKV_ECUDA = 3,    /* a CUDA runtime call failed */
+  OKV_EDEVICE = 4,  /* a kernel recorded an invalid index in the device error word */
+  OKV_ETIMEOUT = 5, /* okv_sync's deadline passed with work still running */
+  OKV_ESTATE = 6    /* call not valid in the context's current state */
+} okv_status;
+
+enum { OKV_F32 = 0, OKV_BF16 = 1 };
+
+typedef struct {
+  int32_t layers;                 /* decoder layers */
+  int32_t q_heads;                /* query heads; a multiple of kv_heads (GQA group g = q/kv) */
+  int32_t kv_heads;               /* KV heads */
+  int32_t head_dim;               /* d: a multiple of 32, at most 256 */
+  int32_t block_size;             /* tokens per KV block (16) */
+  int32_t budget_tokens;          /* KV budget per unit in tokens; Kb = budget/block_size slots */
+  int32_t max_requests;           /* request ids are 0 .. max_requests-1 */
+  int32_t max_blocks_per_request; /* largest context (in blocks) any request may reach */
+  float fetch_cap;                /* default fetch cap, a fraction of the budget (0.05) */
+  int32_t dtype;                  /* OKV_F32 or OKV_BF16 storage for KV, queries, outputs */
+} okv_config;
+
+typedef struct okv_ctx okv_ctx;
+
+/* Create a context on the current CUDA device. Allocates in HBM: block summaries
+ * [layers][max_requests][kv_heads][max_blocks][2][head_dim], the slot pool
+ * [layers][max_requests][kv_heads][Kb][2][block_size][head_dim], the per-unit tables and the
+ * device error word; creates two internal streams. EINVAL on an unsupported config, ENOMEM
+ * if HBM is short. */
+OKV_API okv_status okv_create(const okv_config* cfg, okv_ctx** out);
+/* Waits for the context's work, frees everything it allocated. NULL is a no-op. */
+OKV_API void okv_destroy(okv_ctx* ctx);
+/* Reason for the last failure of a call on ctx ("" if none). */
+OKV_API const char* okv_last_error(const okv_ctx* ctx);
+OKV_API const char* okv_status_string(okv_status s);
+
+/* Page-locked, device-mapped host memory for host KV buffers (cudaHostAlloc). The caller
+ * frees it with okv_host_free. ENOMEM if the host cannot pin that much. */
+OKV_API okv_status okv_host_alloc(int64_t bytes, void** out);
+OKV_API okv_status okv_host_free(void* p);
+
+/* Register request `req` whose full KV stays in host memory ("4 System Design": full KV in
+ * CPU DRAM, compressed summaries in HBM). host_kv: page-locked buffer in the host KV layout
+ * with capacity_blocks blocks per unit; the caller keeps it alive until okv_remove_request.
+ * Builds the min/max summaries of the first n_tokens tokens of every layer by reading the
+ * host buffer (or copies them from an active request registered with the same buffer and
+ * length). The request's slot pool starts empty. EINVAL on bad ids/sizes or unpinned memory,
+ * ESTATE if req is already active. */
+OKV_API okv_status okv_add_request(okv_ctx* ctx, int32_t req, void* host_kv, int32_t capacity_blocks,
+                           int32_t n_tokens, void* stream);
+/* Forget request `req` (its pool slots become free). Synchronises the internal streams. */
+OKV_API okv_status okv_remove_request(okv_ctx* ctx, int32_t req);
+
+/* Append one token per active request to `layer` ("2 Background": the cache must remain
+ * available throughout generation). k_new, v_new: device [max_requests][kv_heads][head_dim];
+ * rows of inactive requests are ignored. Writes the token into the host buffer, into the pool
+ * slot if its block is resident, and updates the block's min/max summary; advances the
+ * layer's length of each active request. Waits for the layer's previous staging. EINVAL if a
+ * request is full or shares its host buffer with another active request. */
+OKV_API okv_status okv_append(okv_ctx* ctx, int32_t layer, const void* k_new, const void* v_new,
+                      void* stream);
+
+/* Next-step prefetch from lookahead ("4 System Design": the per-layer background chain is
+ * top-K prediction, KV selection and KV transfer). draft_q: device [max_requests][q_heads]
+ * [head_dim], the draft query of every active request. Enqueued after the work already on
+ * `stream`, on the context's internal streams:
+ *   scores of every block from its summary, top-Kb blocks per unit (score desc, id asc),
+ *   diff against the resident pool: admit at most C = max(1, floor(cap * Kb)) missing blocks
+ *   per unit, evicting least-recently-selected unselected blocks, stamps = step,
+ *   gather of the admitted blocks from host memory into their slots.
+ * fetch_cap < 0 uses the config's cap. The draft is copied on `stream` before the call returns
+ * control of it, so the caller may overwrite draft_q by work enqueued later on `stream`.
+ * Returns once enqueued; okv_attend on the same layer waits for it. */
+OKV_API okv_status okv_stage(okv_ctx* ctx, int32_t layer, const void* draft_q, int32_t step,
+                     float fetch_cap, void* stream);
+
+/* Sparse attention over the resident set ("4 System Design": attention runs over resident KV
+ * in HBM). q: device [max_requests][q_heads][head_dim]; out: device, same shape and dtype.
+ * For every active request and query head: softmax(q.k / sqrt(d)) v over every valid token of
+ * every occupied slot of its unit (zeros if none). Waits on `stream` for the layer's last
+ * staging. Rows of inactive requests are not written. */
+OKV_API okv_status okv_attend(okv_ctx* ctx, int32_t layer, const void* q, void* out, void* stream);
+
+/* One decode step over every layer, in layer order ("4 System Design": the foreground waits
+ * only for each layer's transfer; the background chain of layer l overlaps the attention of the
+ * later layers): for l = 0 .. layers-1: okv_append(l) if k_new is not NULL, okv_attend(l),
+ * okv_stage(l, step). q, draft_q, out: device [layers][max_requests][q_heads][head_dim];
+ * k_new, v_new: device [layers][max_requests][kv_heads][head_dim] or NULL. Stops at the first
+ * failing call and returns its status. */
+OKV_API okv_status okv_step(okv_ctx* ctx, const void* q, const void* draft_q, void* out,
+                            const void* k_new, const void* v_new, int32_t step, float fetch_cap,
+                            void* stream);
+
+/* Make `stream` wait (on the device, without blocking the host) for all work the context has
+ * enqueued so far on its internal streams: the staging of every layer. */
+OKV_API okv_status okv_join(okv_ctx* ctx, void* stream);
+
+/* Wait (polling, up to timeout_ms; < 0 = no limit) for the context's internal streams and
+ * check the device error word. ETIMEOUT with work still in flight, EDEVICE if a kernel
+ * recorded an invalid index (the word is then cleared). */
+OKV_API okv_status okv_sync(okv_ctx* ctx, int64_t timeout_ms);
+
+/* ---- inspection: synchronise the internal streams, then copy to caller-owned host arrays.
+ * The caller must first synchronise any stream it passed to okv_attend / okv_append. ---- */
+
+/* Summaries of one request: out [kv_heads][max_blocks_per_request][2][head_dim] storage. */
+OKV_API okv_status okv_read_summaries(okv_ctx* ctx, int32_t layer, int32_t req, void* out);
+/* Last selection of a layer: counts [max_requests][kv_heads]; ids and scores
+ * [max_requests][kv_heads][Kb] (first counts[] entries valid). Either array may be NULL. */
+OKV_API okv_status okv_read_selection(okv_ctx* ctx, int32_t layer, int32_t* counts, int32_t* ids,
+                              float* scores);
+/* Slot tables: slot_block [max_requests][kv_heads][Kb] (block id or -1), stamps (same shape). */
+OKV_API okv_status okv_read_slot_table(okv_ctx* ctx, int32_t layer, int32_t* slot_block, int32_t* stamps);
+/* Last fetch lists: counts [max_requests][kv_heads]; entries [max_requests][kv_heads][Kb][2]
+ * as (block id, slot), in admission order. */
+OKV_API okv_status okv_read_fetch_list(okv_ctx* ctx, int32_t layer, int32_t* counts, int32_t* entries);
+/* Pool contents of one unit: out [Kb][2][block_size][head_dim] storage. */
+OKV_API okv_status okv_read_pool(okv_ctx* ctx, int32_t layer, int32_t req, int32_t kv_head, void* out);
+/* Current context length of every request at a layer: lengths [max_requests] (0 if inactive). */
+OKV_API okv_status okv_read_lengths(okv_ctx* ctx, int32_t layer, int32_t* lengths);
+
+/* ---- measurement ---- */
+
+enum {
+  OKV_K_SUMMARY = 0, OKV_K_SCORE_TOPK = 1, OKV_K_SELECT = 2, OKV_K_GATHER = 3, OKV_K_ATTEND = 4,
+  OKV_K_COMBINE = 5, OKV_K_APPEND = 6, OKV_K_COUNT = 7
+};
+
+typedef struct {
+  double ms[OKV_K_COUNT];         /* summed device time of each kernel kind (CUDA events) */
+  int64_t launches[OKV_K_COUNT];  /* kernel launches of each kind */
+  int64_t fetched_blocks;         /* blocks gathered host -> HBM */
+  int64_t attended_slots;         /* occupied slots read by attention launches */
+} okv_timing;
+
+/* Enable (1) or disable (0) per-launch CUDA-event timing; resets the totals. */
+OKV_API okv_status okv_set_timing(okv_ctx* ctx, int32_t enable);
+/* Synchronise and return the totals since okv_set_timing. */
+OKV_API okv_status okv_read_timing(okv_ctx* ctx, okv_timing* out);
+/* Kernel launches made by this context so far (all kinds), counted on the host. */
+OKV_API int64_t okv_launch_count(const okv_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,768 @@
+// C ABI of the okv library: context, requests, the per-layer staging pipeline, inspection and
+// timing. Declarations and contracts are in include/okv.h.
+//
+// Stream layout (OasisKV, paperlayer.ai/abs/2608.08097v1, "4 System Design": the per-layer
+// background chain of top-K prediction, KV selection and KV transfer runs on independent
+// workers overlapped across layers and steps; the foreground waits only for that layer's
+// transfer):
+//   caller stream : [wait staged(l)] attend(l)            [wait staged(l)] append(l)
+//   select stream : [wait caller] [wait staged(l)] score+top-K(l) -> select(l) -> selected(l)
+//   copy stream   : [wait selected(l)] gather(l) -> staged(l)
+// Staging of layer l at step t starts after the work the caller enqueued before it (its
+// attention of layer l at step t, which reads the slots the gather may overwrite), and the
+// attention of layer l at step t+1 waits only for staged(l).
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <chrono>
+#include <thread>
+
+#include "okv_internal.h"
+
+using okv::Counters;
+using okv::Geom;
+using okv::LayerState;
+using okv::ReqTables;
+
+struct TimedLaunch {
+  int kind;
+  cudaEvent_t a, b;
+};
+
+struct okv_ctx {
+  okv_config cfg{};
+  Geom G{};
+  int device = 0;
+  std::string last_error;
+
+  // device state, [layers] x per-layer block
+  uint8_t* summ = nullptr;
+  uint8_t* pool = nullptr;
+  int16_t* resident = nullptr;
+  int32_t* slot_block = nullptr;
+  int32_t* stamp = nullptr;
+  int32_t* sel_ids = nullptr;
+  float* sel_scores = nullptr;
+  int32_t* n_sel = nullptr;
+  int32_t* fetch = nullptr;
+  int32_t* n_fetch = nullptr;
+  int32_t* len = nullptr;
+  int32_t* active_dev = nullptr;
+  uint64_t* host_kv_dev = nullptr;
+  int32_t* cap_dev = nullptr;
+  int32_t* err_dev = nullptr;
+  Counters* ctr_dev = nullptr;
+  void* partials = nullptr;
+  size_t partials_bytes = 0;
+  uint8_t* draft_buf = nullptr;  // [layers][R][Hq][d]: the staging's own copy of the draft queries
+  CUtensorMap pool_map;  // 64-byte aligned by its type
+  bool have_map = false;
+
+  // host mirrors
+  std::vector<int> active;             // [R] 0/1
+  std::vector<int32_t> active_list;    // compact
+  std::vector<void*> host_ptr;         // [R]
+  std::vector<int32_t> cap_blocks;     // [R]
+  std::vector<int32_t> len_host;       // [L][R]
+  std::vector<int> shared_buf;         // [R] host buffer shared with another active request
+
+  // streams and events
+  cudaStream_t sel_stream = nullptr, copy_stream = nullptr;
+  cudaEvent_t ev_in = nullptr;
+  std::vector<cudaEvent_t> ev_selected, ev_staged;
+  std::vector<char> staged_once;
+
+  // timing
+  bool timing = false;
+  std::vector<TimedLaunch> pending;
+  std::vector<cudaEvent_t> event_pool;
+  double ms[OKV_K_COUNT] = {};
+  int64_t n_launch_kind[OKV_K_COUNT] = {};
+  int64_t launches = 0;
+
+  // sizes
+  int64_t per_layer_units = 0;
+  int64_t summ_layer_bytes = 0, pool_layer_bytes = 0;
+};
+
+namespace {
+
+okv_status fail(okv_ctx* ctx, okv_status st, const char* fmt, ...) {
+  if (ctx) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    ctx->last_error = buf;
+  }
+  return st;
+}
+
+#define OKV_CUDA(ctx, call)                                                                    \
+  do {                                                                                         \
+    cudaError_t e_ = (call);                                                                   \
+    if (e_ != cudaSuccess)                                                                     \
+      return fail(ctx, e_ == cudaErrorMemoryAllocation ? OKV_ENOMEM : OKV_ECUDA, "%s: %s (%s:%d)", \
+                  #call, cudaGetErrorString(e_), __FILE__, __LINE__);                          \
+  } while (0)
+
+LayerState layer_state(const okv_ctx* c, int32_t layer) {
+  const Geom& G = c->G;
+  const int64_t U = c->per_layer_units;
+  LayerState S;
+  S.summ = c->summ + layer * c->summ_layer_bytes;
+  S.pool = c->pool + layer * c->pool_layer_bytes;
+  S.resident = c->resident + layer * U * G.nb_max;
+  S.slot_block = c->slot_block + layer * U * G.kb;
+  S.stamp = c->stamp + layer * U * G.kb;
+  S.sel_ids = c->sel_ids + layer * U * G.kb;
+  S.sel_scores = c->sel_scores + layer * U * G.kb;
+  S.n_sel = c->n_sel + layer * U;
+  S.fetch = c->fetch + layer * U * G.kb * 2;
+  S.n_fetch = c->n_fetch + layer * U;
+  S.len = c->len + (int64_t)layer * G.R;
+  return S;
+}
+
+ReqTables req_tables(const okv_ctx* c) {
+  ReqTables T;
+  T.active = c->active_dev;
+  T.host_kv = c->host_kv_dev;
+  T.cap_blocks = c->cap_dev;
+  return T;
+}
+
+int32_t cap_to_blocks(float cap, int32_t kb) {
+  double c = floor((double)cap * (double)kb);
+  if (c < 1.0) c = 1.0;
+  if (c > kb) c = kb;
+  return (int32_t)c;
+}
+
+// Timing: a pair of events around one launch on `s`.
+struct Timer {
+  okv_ctx* c;
+  int kind;
+  cudaStream_t s;
+  cudaEvent_t a = nullptr, b = nullptr;
+  Timer(okv_ctx* c_, int k, cudaStream_t s_) : c(c_), kind(k), s(s_) {
+    if (!c->timing) return;
+    a = take();
+    b = take();
+    if (a && b) cudaEventRecord(a, s);
+  }
+  cudaEvent_t take() {
+    if (!c->event_pool.empty()) {
+      cudaEvent_t e = c->event_pool.back();
+      c->event_pool.pop_back();
+      return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+  }
+  void stop(int n_launches) {
+    c->launches += n_launches;
+    c->n_launch_kind[kind] += n_launches;
+    if (!c->timing || !a || !b) return;
+    cudaEventRecord(b, s);
+    c->pending.push_back({kind, a, b});
+  }
+};
+
+okv_status check_device_error(okv_ctx* c) {
+  int32_t e[4];
+  OKV_CUDA(c, cudaMemcpy(e, c->err_dev, sizeof(e), cudaMemcpyDeviceToHost));
+  if (e[0] != 0) {
+    static const int32_t zero[4] = {0, 0, 0, 0};
+    cudaMemcpy(c->err_dev, zero, sizeof(zero), cudaMemcpyHostToDevice);
+    static const char* names[] = {"none", "block id out of range", "slot out of range",
+                                  "append past capacity", "context length out of range",
+                                  "asynchronous copy wait timed out"};
+    const char* n = (e[0] >= 0 && e[0] <= 5) ? names[e[0]] : "unknown";
+    return fail(c, OKV_EDEVICE, "device error %d (%s): layer/site %d, request %d, value %d", e[0], n,
+                e[1], e[2], e[3]);
+  }
+  return OKV_OK;
+}
+
+okv_status sync_internal(okv_ctx* c) {
+  OKV_CUDA(c, cudaStreamSynchronize(c->sel_stream));
+  OKV_CUDA(c, cudaStreamSynchronize(c->copy_stream));
+  return OKV_OK;
+}
+
+okv_status upload_active(okv_ctx* c) {
+  c->active_list.clear();
+  for (int32_t r = 0; r < c->G.R; ++r)
+    if (c->active[r]) c->active_list.push_back(r);
+  if (!c->active_list.empty())
+    OKV_CUDA(c, cudaMemcpy(c->active_dev, c->active_list.data(), c->active_list.size() * sizeof(int32_t),
+                           cudaMemcpyHostToDevice));
+  // shared host buffers among active requests
+  for (int32_t r = 0; r < c->G.R; ++r) c->shared_buf[r] = 0;
+  for (size_t i = 0; i < c->active_list.size(); ++i)
+    for (size_t j = i + 1; j < c->active_list.size(); ++j)
+      if (c->host_ptr[c->active_list[i]] == c->host_ptr[c->active_list[j]])
+        c->shared_buf[c->active_list[i]] = c->shared_buf[c->active_list[j]] = 1;
+  return OKV_OK;
+}
+
+int32_t max_blocks_at(const okv_ctx* c, int32_t layer) {
+  int32_t m = 0;
+  for (int32_t r : c->active_list) {
+    const int32_t nb = (c->len_host[(size_t)layer * c->G.R + r] + c->G.bs - 1) / c->G.bs;
+    if (nb > m) m = nb;
+  }
+  return m;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* okv_status_string(okv_status s) {
+  switch (s) {
+    case OKV_OK: return "ok";
+    case OKV_EINVAL: return "invalid argument";
+    case OKV_ENOMEM: return "out of memory";
+    case OKV_ECUDA: return "CUDA error";
+    case OKV_EDEVICE: return "device error";
+    case OKV_ETIMEOUT: return "timeout";
+    case OKV_ESTATE: return "invalid state";
+  }
+  return "unknown status";
+}
+
+const char* okv_last_error(const okv_ctx* ctx) { return ctx ? ctx->last_error.c_str() : ""; }
+
+okv_status okv_host_alloc(int64_t bytes, void** out) {
+  if (!out || bytes <= 0) return OKV_EINVAL;
+  *out = nullptr;
+  cudaError_t e = cudaHostAlloc(out, (size_t)bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+  if (e != cudaSuccess) {
+    *out = nullptr;
+    return e == cudaErrorMemoryAllocation ? OKV_ENOMEM : OKV_ECUDA;
+  }
+  return OKV_OK;
+}
+
+okv_status okv_host_free(void* p) {
+  if (!p) return OKV_OK;
+  return cudaFreeHost(p) == cudaSuccess ? OKV_OK : OKV_ECUDA;
+}
+
+void okv_destroy(okv_ctx* c) {
+  if (!c) return;
+  if (c->sel_stream) cudaStreamSynchronize(c->sel_stream);
+  if (c->copy_stream) cudaStreamSynchronize(c->copy_stream);
+  for (auto& t : c->pending) {
+    cudaEventDestroy(t.a);
+    cudaEventDestroy(t.b);
+  }
+  for (auto e : c->event_pool) cudaEventDestroy(e);
+  for (auto e : c->ev_selected) if (e) cudaEventDestroy(e);
+  for (auto e : c->ev_staged) if (e) cudaEventDestroy(e);
+  if (c->ev_in) cudaEventDestroy(c->ev_in);
+  if (c->sel_stream) cudaStreamDestroy(c->sel_stream);
+  if (c->copy_stream) cudaStreamDestroy(c->copy_stream);
+  void* bufs[] = {c->summ, c->pool, c->resident, c->slot_block, c->stamp, c->sel_ids, c->sel_scores,
+                  c->n_sel, c->fetch, c->n_fetch, c->len, c->active_dev, c->host_kv_dev, c->cap_dev,
+                  c->err_dev, c->ctr_dev, c->partials, c->draft_buf};
+  for (void* p : bufs)
+    if (p) cudaFree(p);
+  delete c;
+}
+
+okv_status okv_create(const okv_config* cfg, okv_ctx** out) {
+  if (!cfg || !out) return OKV_EINVAL;
+  *out = nullptr;
+  const okv_config& k = *cfg;
+  okv_ctx* c = new okv_ctx();
+  auto bad = [&](const char* why) {
+    okv_status st = fail(c, OKV_EINVAL, "okv_create: %s", why);
+    fprintf(stderr, "okv_create: %s\n", why);
+    delete c;
+    return st;
+  };
+  if (k.layers <= 0 || k.q_heads <= 0 || k.kv_heads <= 0 || k.q_heads % k.kv_heads) return bad("heads");
+  if (k.head_dim <= 0 || k.head_dim % 32 || k.head_dim > 256) return bad("head_dim must be a multiple of 32, at most 256");
+  if (k.q_heads / k.kv_heads > 8) return bad("GQA group larger than 8");
+  if (k.block_size <= 0 || k.block_size > 64) return bad("block_size must be in 1..64");
+  if (k.budget_tokens < k.block_size || k.budget_tokens % k.block_size) return bad("budget must be a multiple of block_size");
+  if (k.budget_tokens / k.block_size > 1024) return bad("at most 1024 slots per unit");
+  if (k.max_requests <= 0 || k.max_blocks_per_request <= 0) return bad("sizes");
+  if (k.max_blocks_per_request > 32767) return bad("max_blocks_per_request must fit the int16 resident map");
+  if (!(k.fetch_cap > 0.f) || k.fetch_cap > 1.f) return bad("fetch_cap must be in (0, 1]");
+  if (k.dtype != OKV_F32 && k.dtype != OKV_BF16) return bad("dtype");
+  c->cfg = k;
+  Geom& G = c->G;
+  G.L = k.layers;
+  G.Hq = k.q_heads;
+  G.Hkv = k.kv_heads;
+  G.g = k.q_heads / k.kv_heads;
+  G.d = k.head_dim;
+  G.bs = k.block_size;
+  G.kb = k.budget_tokens / k.block_size;
+  G.R = k.max_requests;
+  G.nb_max = k.max_blocks_per_request;
+  G.dtype = k.dtype;
+  G.elem = k.dtype == OKV_F32 ? 4 : 2;
+  G.block_bytes = (int64_t)2 * G.bs * G.d * G.elem;
+  if ((G.bs * G.d * G.elem) % 16) return bad("block rows must be a multiple of 16 bytes");
+
+  okv_status st = OKV_OK;
+  auto alloc = [&](void** p, size_t bytes) -> bool {
+    cudaError_t e = cudaMalloc(p, bytes ? bytes : 16);
+    if (e != cudaSuccess) {
+      st = fail(c, e == cudaErrorMemoryAllocation ? OKV_ENOMEM : OKV_ECUDA, "cudaMalloc(%zu): %s", bytes,
+                cudaGetErrorString(e));
+      return false;
+    }
+    return true;
+  };
+  cudaGetDevice(&c->device);
+  const int64_t U = (int64_t)G.R * G.Hkv;
+  c->per_layer_units = U;
+  c->summ_layer_bytes = U * G.nb_max * 2 * G.d * G.elem;
+  c->pool_layer_bytes = U * G.kb * G.block_bytes;
+  const int64_t L = G.L;
+  bool ok = alloc((void**)&c->summ, L * c->summ_layer_bytes) && alloc((void**)&c->pool, L * c->pool_layer_bytes) &&
+            alloc((void**)&c->resident, L * U * G.nb_max * sizeof(int16_t)) &&
+            alloc((void**)&c->slot_block, L * U * G.kb * 4) && alloc((void**)&c->stamp, L * U * G.kb * 4) &&
+            alloc((void**)&c->sel_ids, L * U * G.kb * 4) && alloc((void**)&c->sel_scores, L * U * G.kb * 4) &&
+            alloc((void**)&c->n_sel, L * U * 4) && alloc((void**)&c->fetch, L * U * G.kb * 8) &&
+            alloc((void**)&c->n_fetch, L * U * 4) && alloc((void**)&c->len, L * G.R * 4) &&
+            alloc((void**)&c->active_dev, G.R * 4) && alloc((void**)&c->host_kv_dev, G.R * 8) &&
+            alloc((void**)&c->cap_dev, G.R * 4) && alloc((void**)&c->err_dev, 16) &&
+            alloc((void**)&c->ctr_dev, sizeof(Counters)) &&
+            alloc((void**)&c->draft_buf, (size_t)L * G.R * G.Hq * G.d * G.elem);
+  if (ok) {
+    size_t ws = 0;
+    for (int32_t n = 1; n <= G.R; ++n) {
+      const size_t w = okv::attend_workspace_bytes(G, n);
+      if (w > ws) ws = w;
+    }
+    c->partials_bytes = ws;
+    ok = alloc(&c->partials, ws);
+  }
+  if (!ok) {
+    fprintf(stderr, "okv_create: %s\n", c->last_error.c_str());
+    okv_destroy(c);
+    return st;
+  }
+  auto ck = [&](cudaError_t e) {
+    if (e != cudaSuccess && st == OKV_OK) st = fail(c, OKV_ECUDA, "okv_create: %s", cudaGetErrorString(e));
+  };
+  ck(cudaMemset(c->resident, 0xFF, L * U * G.nb_max * sizeof(int16_t)));
+  ck(cudaMemset(c->slot_block, 0xFF, L * U * G.kb * 4));
+  ck(cudaMemset(c->stamp, 0xFF, L * U * G.kb * 4));
+  ck(cudaMemset(c->n_sel, 0, L * U * 4));
+  ck(cudaMemset(c->n_fetch, 0, L * U * 4));
+  ck(cudaMemset(c->len, 0, L * G.R * 4));
+  ck(cudaMemset(c->err_dev, 0, 16));
+  ck(cudaMemset(c->ctr_dev, 0, sizeof(Counters)));
+  ck(cudaMemset(c->host_kv_dev, 0, G.R * 8));
+  ck(cudaMemset(c->cap_dev, 0, G.R * 4));
+  int lo = 0, hi = 0;
+  ck(cudaDeviceGetStreamPriorityRange(&lo, &hi));
+  ck(cudaStreamCreateWithPriority(&c->sel_stream, cudaStreamNonBlocking, lo));
+  ck(cudaStreamCreateWithPriority(&c->copy_stream, cudaStreamNonBlocking, lo));
+  ck(cudaEventCreateWithFlags(&c->ev_in, cudaEventDisableTiming));
+  c->ev_selected.assign(G.L, nullptr);
+  c->ev_staged.assign(G.L, nullptr);
+  c->staged_once.assign(G.L, 0);
+  for (int32_t l = 0; l < G.L; ++l) {
+    ck(cudaEventCreateWithFlags(&c->ev_selected[l], cudaEventDisableTiming));
+    ck(cudaEventCreateWithFlags(&c->ev_staged[l], cudaEventDisableTiming));
+  }
+  c->active.assign(G.R, 0);
+  c->host_ptr.assign(G.R, nullptr);
+  c->cap_blocks.assign(G.R, 0);
+  c->len_host.assign((size_t)G.L * G.R, 0);
+  c->shared_buf.assign(G.R, 0);
+
+  if (st == OKV_OK && okv::attend_uses_tensor_cores(G)) {
+    // pool as rows of 256 bytes: dims {64 elements, 2 halves, rows}, box = one slot (32 rows)
+    const uint64_t rows = (uint64_t)L * U * G.kb * 32;
+    if (rows >= (1ull << 31)) {
+      st = fail(c, OKV_EINVAL, "okv_create: slot pool too large for 32-bit TMA row coordinates");
+    } else {
+      typedef CUresult (*EncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+      if (e != cudaSuccess || !fn || q != cudaDriverEntryPointSuccess) {
+        st = fail(c, OKV_ECUDA, "okv_create: cuTensorMapEncodeTiled unavailable");
+      } else {
+        const cuuint64_t dims[3] = {64, 2, rows};
+        const cuuint64_t strides[2] = {128, 256};
+        const cuuint32_t box[3] = {64, 2, 32};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        CUresult r = ((EncodeFn)fn)(&c->pool_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, c->pool, dims, strides, box,
+                                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS)
+          st = fail(c, OKV_ECUDA, "okv_create: cuTensorMapEncodeTiled failed (%d)", (int)r);
+        else
+          c->have_map = true;
+      }
+    }
+  }
+  if (st == OKV_OK) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) st = fail(c, OKV_ECUDA, "okv_create: %s", cudaGetErrorString(e));
+  }
+  if (st != OKV_OK) {
+    fprintf(stderr, "okv_create: %s\n", c->last_error.c_str());
+    okv_destroy(c);
+    return st;
+  }
+  *out = c;
+  return OKV_OK;
+}
+
+okv_status okv_add_request(okv_ctx* c, int32_t req, void* host_kv, int32_t capacity_blocks,
+                           int32_t n_tokens, void* stream) {
+  if (!c) return OKV_EINVAL;
+  const Geom& G = c->G;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (req < 0 || req >= G.R) return fail(c, OKV_EINVAL, "okv_add_request: request id %d out of range", req);
+  if (c->active[req]) return fail(c, OKV_ESTATE, "okv_add_request: request %d is already active", req);
+  if (!host_kv) return fail(c, OKV_EINVAL, "okv_add_request: host_kv is NULL");
+  if (capacity_blocks <= 0 || capacity_blocks > G.nb_max)
+    return fail(c, OKV_EINVAL, "okv_add_request: capacity_blocks %d not in 1..%d", capacity_blocks, G.nb_max);
+  if (n_tokens < 0 || (int64_t)n_tokens > (int64_t)capacity_blocks * G.bs)
+    return fail(c, OKV_EINVAL, "okv_add_request: n_tokens %d exceeds the capacity", n_tokens);
+  // page-locked host memory only (on address-translation systems pageable memory would also be
+  // reachable, but at the mercy of the OS pager)
+  cudaPointerAttributes attr{};
+  void* dptr = nullptr;
+  if (cudaPointerGetAttributes(&attr, host_kv) != cudaSuccess || attr.type != cudaMemoryTypeHost ||
+      cudaHostGetDevicePointer(&dptr, host_kv, 0) != cudaSuccess || !dptr) {
+    cudaGetLastError();
+    return fail(c, OKV_EINVAL, "okv_add_request: host_kv is not page-locked, device-mapped memory");
+  }
+  if ((reinterpret_cast<uintptr_t>(dptr) & 15) != 0) return fail(c, OKV_EINVAL, "okv_add_request: host_kv must be 16-byte aligned");
+  // every earlier use of the context's tables must be complete before they are reset
+  if (okv_status st = sync_internal(c)) return st;
+  OKV_CUDA(c, cudaStreamSynchronize(s));
+
+  // an active request registered with the same buffer and length has identical summaries
+  int32_t twin = -1;
+  for (int32_t r : c->active_list) {
+    if (c->host_ptr[r] != host_kv || c->cap_blocks[r] != capacity_blocks) continue;
+    bool same = true;
+    for (int32_t l = 0; l < G.L && same; ++l) same = c->len_host[(size_t)l * G.R + r] == n_tokens;
+    if (same) {
+      twin = r;
+      break;
+    }
+  }
+  OKV_CUDA(c, okv::launch_reset_request(G, c->resident, c->slot_block, c->stamp, c->n_sel, c->n_fetch, c->len, req,
+                                        n_tokens, (uint64_t)(uintptr_t)dptr, capacity_blocks, c->host_kv_dev,
+                                        c->cap_dev, s));
+  c->launches += 1;
+  if (twin >= 0) {
+    const size_t bytes = (size_t)G.Hkv * G.nb_max * 2 * G.d * G.elem;
+    for (int32_t l = 0; l < G.L; ++l) {
+      uint8_t* base = c->summ + l * c->summ_layer_bytes;
+      OKV_CUDA(c, cudaMemcpyAsync(base + (size_t)req * bytes, base + (size_t)twin * bytes, bytes,
+                                  cudaMemcpyDeviceToDevice, s));
+    }
+  } else {
+    Timer t(c, OKV_K_SUMMARY, s);
+    OKV_CUDA(c, okv::launch_summary_build(G, 0, G.L, req, (uint64_t)(uintptr_t)dptr, capacity_blocks, n_tokens,
+                                          c->summ, c->err_dev, s));
+    t.stop(n_tokens > 0 ? 1 : 0);
+  }
+  OKV_CUDA(c, cudaStreamSynchronize(s));
+  c->active[req] = 1;
+  c->host_ptr[req] = host_kv;
+  c->cap_blocks[req] = capacity_blocks;
+  for (int32_t l = 0; l < G.L; ++l) c->len_host[(size_t)l * G.R + req] = n_tokens;
+  if (okv_status st = upload_active(c)) return st;
+  return check_device_error(c);
+}
+
+okv_status okv_remove_request(okv_ctx* c, int32_t req) {
+  if (!c) return OKV_EINVAL;
+  if (req < 0 || req >= c->G.R) return fail(c, OKV_EINVAL, "okv_remove_request: request id %d out of range", req);
+  if (!c->active[req]) return fail(c, OKV_ESTATE, "okv_remove_request: request %d is not active", req);
+  if (okv_status st = sync_internal(c)) return st;
+  OKV_CUDA(c, cudaDeviceSynchronize());
+  c->active[req] = 0;
+  c->host_ptr[req] = nullptr;
+  for (int32_t l = 0; l < c->G.L; ++l) c->len_host[(size_t)l * c->G.R + req] = 0;
+  return upload_active(c);
+}
+
+okv_status okv_append(okv_ctx* c, int32_t layer, const void* k_new, const void* v_new, void* stream) {
+  if (!c) return OKV_EINVAL;
+  const Geom& G = c->G;
+  if (layer < 0 || layer >= G.L) return fail(c, OKV_EINVAL, "okv_append: layer %d out of range", layer);
+  if (!k_new || !v_new) return fail(c, OKV_EINVAL, "okv_append: NULL input");
+  for (int32_t r : c->active_list) {
+    if (c->shared_buf[r])
+      return fail(c, OKV_EINVAL, "okv_append: request %d shares its host buffer with another active request", r);
+    const int32_t n = c->len_host[(size_t)layer * G.R + r];
+    if ((int64_t)n >= (int64_t)c->cap_blocks[r] * G.bs)
+      return fail(c, OKV_EINVAL, "okv_append: request %d is full at layer %d", r, layer);
+  }
+  const int32_t n_active = (int32_t)c->active_list.size();
+  if (n_active == 0) return OKV_OK;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (c->staged_once[layer]) OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_staged[layer], 0));
+  const LayerState S = layer_state(c, layer);
+  const ReqTables T = req_tables(c);
+  Timer t(c, OKV_K_APPEND, s);
+  OKV_CUDA(c, okv::launch_append(G, S, T, n_active, layer, k_new, v_new, c->err_dev, s));
+  OKV_CUDA(c, okv::launch_advance(S, T, n_active, s));
+  t.stop(2);
+  for (int32_t r : c->active_list) c->len_host[(size_t)layer * G.R + r] += 1;
+  return OKV_OK;
+}
+
+okv_status okv_stage(okv_ctx* c, int32_t layer, const void* draft_q, int32_t step, float fetch_cap,
+                     void* stream) {
+  if (!c) return OKV_EINVAL;
+  const Geom& G = c->G;
+  if (layer < 0 || layer >= G.L) return fail(c, OKV_EINVAL, "okv_stage: layer %d out of range", layer);
+  if (!draft_q) return fail(c, OKV_EINVAL, "okv_stage: NULL draft query");
+  const float cap = fetch_cap < 0.f ? c->cfg.fetch_cap : fetch_cap;
+  if (!(cap > 0.f) || cap > 1.f) return fail(c, OKV_EINVAL, "okv_stage: fetch cap %g not in (0, 1]", cap);
+  const int32_t C = cap_to_blocks(cap, G.kb);
+  const int32_t n_active = (int32_t)c->active_list.size();
+  if (n_active == 0) return OKV_OK;
+  cudaStream_t s = (cudaStream_t)stream;
+  // the staging reads the draft later, on the select stream: take a copy on the caller's stream
+  // (after the previous staging of this layer has read its copy) so the caller may reuse its buffer
+  const size_t qbytes = (size_t)G.R * G.Hq * G.d * G.elem;
+  uint8_t* draft_copy = c->draft_buf + (size_t)layer * qbytes;
+  if (c->staged_once[layer]) OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_selected[layer], 0));
+  OKV_CUDA(c, cudaMemcpyAsync(draft_copy, draft_q, qbytes, cudaMemcpyDeviceToDevice, s));
+  OKV_CUDA(c, cudaEventRecord(c->ev_in, s));
+  OKV_CUDA(c, cudaStreamWaitEvent(c->sel_stream, c->ev_in, 0));
+  if (c->staged_once[layer]) OKV_CUDA(c, cudaStreamWaitEvent(c->sel_stream, c->ev_staged[layer], 0));
+  const LayerState S = layer_state(c, layer);
+  const ReqTables T = req_tables(c);
+  {
+    Timer t(c, OKV_K_SCORE_TOPK, c->sel_stream);
+    OKV_CUDA(c, okv::launch_score_topk(G, S, T, n_active, max_blocks_at(c, layer), draft_copy, c->err_dev,
+                                       c->sel_stream));
+    t.stop(1);
+  }
+  {
+    Timer t(c, OKV_K_SELECT, c->sel_stream);
+    OKV_CUDA(c, okv::launch_select(G, S, T, n_active, C, step, c->ctr_dev, c->err_dev, c->sel_stream));
+    t.stop(1);
+  }
+  OKV_CUDA(c, cudaEventRecord(c->ev_selected[layer], c->sel_stream));
+  OKV_CUDA(c, cudaStreamWaitEvent(c->copy_stream, c->ev_selected[layer], 0));
+  {
+    Timer t(c, OKV_K_GATHER, c->copy_stream);
+    OKV_CUDA(c, okv::launch_gather(G, S, T, n_active, layer, C, c->err_dev, c->copy_stream));
+    t.stop(1);
+  }
+  OKV_CUDA(c, cudaEventRecord(c->ev_staged[layer], c->copy_stream));
+  c->staged_once[layer] = 1;
+  return OKV_OK;
+}
+
+okv_status okv_attend(okv_ctx* c, int32_t layer, const void* q, void* out, void* stream) {
+  if (!c) return OKV_EINVAL;
+  const Geom& G = c->G;
+  if (layer < 0 || layer >= G.L) return fail(c, OKV_EINVAL, "okv_attend: layer %d out of range", layer);
+  if (!q || !out) return fail(c, OKV_EINVAL, "okv_attend: NULL pointer");
+  const int32_t n_active = (int32_t)c->active_list.size();
+  if (n_active == 0) return OKV_OK;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (c->staged_once[layer]) OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_staged[layer], 0));
+  const LayerState S = layer_state(c, layer);
+  const ReqTables T = req_tables(c);
+  int n_launch = 0, split = 0;
+  Timer t(c, OKV_K_ATTEND, s);
+  OKV_CUDA(c, okv::launch_attend(G, S, T, n_active, layer, q, out, c->have_map ? &c->pool_map : nullptr,
+                                 c->partials, c->ctr_dev, c->err_dev, s, &n_launch, &split));
+  t.stop(n_launch);
+  return OKV_OK;
+}
+
+okv_status okv_step(okv_ctx* c, const void* q, const void* draft_q, void* out, const void* k_new,
+                    const void* v_new, int32_t step, float fetch_cap, void* stream) {
+  if (!c) return OKV_EINVAL;
+  if (!q || !draft_q || !out) return fail(c, OKV_EINVAL, "okv_step: NULL pointer");
+  if ((k_new == nullptr) != (v_new == nullptr)) return fail(c, OKV_EINVAL, "okv_step: k_new and v_new go together");
+  const Geom& G = c->G;
+  const size_t qbytes = (size_t)G.R * G.Hq * G.d * G.elem;
+  const size_t kvbytes = (size_t)G.R * G.Hkv * G.d * G.elem;
+  for (int32_t l = 0; l < G.L; ++l) {
+    if (k_new) {
+      okv_status st = okv_append(c, l, (const uint8_t*)k_new + l * kvbytes, (const uint8_t*)v_new + l * kvbytes, stream);
+      if (st != OKV_OK) return st;
+    }
+    okv_status st = okv_attend(c, l, (const uint8_t*)q + l * qbytes, (uint8_t*)out + l * qbytes, stream);
+    if (st != OKV_OK) return st;
+    st = okv_stage(c, l, (const uint8_t*)draft_q + l * qbytes, step, fetch_cap, stream);
+    if (st != OKV_OK) return st;
+  }
+  return OKV_OK;
+}
+
+okv_status okv_join(okv_ctx* c, void* stream) {
+  if (!c) return OKV_EINVAL;
+  cudaStream_t s = (cudaStream_t)stream;
+  OKV_CUDA(c, cudaEventRecord(c->ev_in, c->sel_stream));
+  OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_in, 0));
+  OKV_CUDA(c, cudaEventRecord(c->ev_in, c->copy_stream));
+  OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_in, 0));
+  return OKV_OK;
+}
+
+okv_status okv_sync(okv_ctx* c, int64_t timeout_ms) {
+  if (!c) return OKV_EINVAL;
+  cudaEvent_t ea = nullptr, eb = nullptr;
+  OKV_CUDA(c, cudaEventCreateWithFlags(&ea, cudaEventDisableTiming));
+  OKV_CUDA(c, cudaEventCreateWithFlags(&eb, cudaEventDisableTiming));
+  OKV_CUDA(c, cudaEventRecord(ea, c->sel_stream));
+  OKV_CUDA(c, cudaEventRecord(eb, c->copy_stream));
+  const auto t0 = std::chrono::steady_clock::now();
+  okv_status st = OKV_OK;
+  for (;;) {
+    const cudaError_t qa = cudaEventQuery(ea), qb = cudaEventQuery(eb);
+    if (qa == cudaSuccess && qb == cudaSuccess) break;
+    if ((qa != cudaSuccess && qa != cudaErrorNotReady) || (qb != cudaSuccess && qb != cudaErrorNotReady)) {
+      st = fail(c, OKV_ECUDA, "okv_sync: %s", cudaGetErrorString(qa != cudaSuccess && qa != cudaErrorNotReady ? qa : qb));
+      break;
+    }
+    const auto ms = std::chrono::duration_cast<std::chrono::milliseconds>(std::chrono::steady_clock::now() - t0).count();
+    if (timeout_ms >= 0 && ms > timeout_ms) {
+      st = fail(c, OKV_ETIMEOUT, "okv_sync: work still running after %lld ms", (long long)timeout_ms);
+      break;
+    }
+    std::this_thread::sleep_for(std::chrono::microseconds(50));
+  }
+  cudaEventDestroy(ea);
+  cudaEventDestroy(eb);
+  if (st != OKV_OK) return st;
+  return check_device_error(c);
+}
+
+okv_status okv_read_summaries(okv_ctx* c, int32_t layer, int32_t req, void* out) {
+  if (!c || !out) return OKV_EINVAL;
+  const Geom& G = c->G;
+  if (layer < 0 || layer >= G.L || req < 0 || req >= G.R) return fail(c, OKV_EINVAL, "okv_read_summaries: range");
+  if (okv_status st = sync_internal(c)) return st;
+  const size_t bytes = (size_t)G.Hkv * G.nb_max * 2 * G.d * G.elem;
+  OKV_CUDA(c, cudaMemcpy(out, c->summ + layer * c->summ_layer_bytes + (size_t)req * bytes, bytes, cudaMemcpyDeviceToHost));
+  return check_device_error(c);
+}
+
+okv_status okv_read_selection(okv_ctx* c, int32_t layer, int32_t* counts, int32_t* ids, float* scores) {
+  if (!c) return OKV_EINVAL;
+  const Geom& G = c->G;
+  if (layer < 0 || layer >= G.L) return fail(c, OKV_EINVAL, "okv_read_selection: layer out of range");
+  if (okv_status st = sync_internal(c)) return st;
+  const LayerState S = layer_state(c, layer);
+  const int64_t U = c->per_layer_units;
+  if (counts) OKV_CUDA(c, cudaMemcpy(counts, S.n_sel, U * 4, cudaMemcpyDeviceToHost));
+  if (ids) OKV_CUDA(c, cudaMemcpy(ids, S.sel_ids, U * G.kb * 4, cudaMemcpyDeviceToHost));
+  if (scores) OKV_CUDA(c, cudaMemcpy(scores, S.sel_scores, U * G.kb * 4, cudaMemcpyDeviceToHost));
+  return check_device_error(c);
+}
+
+okv_status okv_read_slot_table(okv_ctx* c, int32_t layer, int32_t* slot_block, int32_t* stamps) {
+  if (!c) return OKV_EINVAL;
+  const Geom& G = c->G;
+  if (layer < 0 || layer >= G.L) return fail(c, OKV_EINVAL, "okv_read_slot_table: layer out of range");
+  if (okv_status st = sync_internal(c)) return st;
+  const LayerState S = layer_state(c, layer);
+  const int64_t U = c->per_layer_units;
+  if (slot_block) OKV_CUDA(c, cudaMemcpy(slot_block, S.slot_block, U * G.kb * 4, cudaMemcpyDeviceToHost));
+  if (stamps) OKV_CUDA(c, cudaMemcpy(stamps, S.stamp, U * G.kb * 4, cudaMemcpyDeviceToHost));
+  return check_device_error(c);
+}
+
+okv_status okv_read_fetch_list(okv_ctx* c, int32_t layer, int32_t* counts, int32_t* entries) {
+  if (!c) return OKV_EINVAL;
+  const Geom& G = c->G;
+  if (layer < 0 || layer >= G.L) return fail(c, OKV_EINVAL, "okv_read_fetch_list: layer out of range");
+  if (okv_status st = sync_internal(c)) return st;
+  const LayerState S = layer_state(c, layer);
+  const int64_t U = c->per_layer_units;
+  if (counts) OKV_CUDA(c, cudaMemcpy(counts, S.n_fetch, U * 4, cudaMemcpyDeviceToHost));
+  if (entries) OKV_CUDA(c, cudaMemcpy(entries, S.fetch, U * G.kb * 8, cudaMemcpyDeviceToHost));
+  return check_device_error(c);
+}
+
+okv_status okv_read_pool(okv_ctx* c, int32_t layer, int32_t req, int32_t kv_head, void* out) {
+  if (!c || !out) return OKV_EINVAL;
+  const Geom& G = c->G;
+  if (layer < 0 || layer >= G.L || req < 0 || req >= G.R || kv_head < 0 || kv_head >= G.Hkv)
+    return fail(c, OKV_EINVAL, "okv_read_pool: range");
+  if (okv_status st = sync_internal(c)) return st;
+  const LayerState S = layer_state(c, layer);
+  const size_t bytes = (size_t)G.kb * G.block_bytes;
+  OKV_CUDA(c, cudaMemcpy(out, S.pool + ((size_t)req * G.Hkv + kv_head) * bytes, bytes, cudaMemcpyDeviceToHost));
+  return check_device_error(c);
+}
+
+okv_status okv_read_lengths(okv_ctx* c, int32_t layer, int32_t* lengths) {
+  if (!c || !lengths) return OKV_EINVAL;
+  const Geom& G = c->G;
+  if (layer < 0 || layer >= G.L) return fail(c, OKV_EINVAL, "okv_read_lengths: layer out of range");
+  if (okv_status st = sync_internal(c)) return st;
+  OKV_CUDA(c, cudaMemcpy(lengths, c->len + (size_t)layer * G.R, G.R * 4, cudaMemcpyDeviceToHost));
+  for (int32_t r = 0; r < G.R; ++r)
+    if (!c->active[r]) lengths[r] = 0;
+  return check_device_error(c);
+}
+
+okv_status okv_set_timing(okv_ctx* c, int32_t enable) {
+  if (!c) return OKV_EINVAL;
+  if (okv_status st = sync_internal(c)) return st;
+  OKV_CUDA(c, cudaDeviceSynchronize());
+  for (auto& t : c->pending) {
+    c->event_pool.push_back(t.a);
+    c->event_pool.push_back(t.b);
+  }
+  c->pending.clear();
+  for (int k = 0; k < OKV_K_COUNT; ++k) {
+    c->ms[k] = 0.0;
+    c->n_launch_kind[k] = 0;
+  }
+  OKV_CUDA(c, cudaMemset(c->ctr_dev, 0, sizeof(Counters)));
+  c->timing = enable != 0;
+  return OKV_OK;
+}
+
+okv_status okv_read_timing(okv_ctx* c, okv_timing* out) {
+  if (!c || !out) return OKV_EINVAL;
+  for (auto& t : c->pending) {
+    OKV_CUDA(c, cudaEventSynchronize(t.b));
+    float ms = 0.f;
+    OKV_CUDA(c, cudaEventElapsedTime(&ms, t.a, t.b));
+    c->ms[t.kind] += ms;
+    c->event_pool.push_back(t.a);
+    c->event_pool.push_back(t.b);
+  }
+  c->pending.clear();
+  Counters h{};
+  OKV_CUDA(c, cudaMemcpy(&h, c->ctr_dev, sizeof(h), cudaMemcpyDeviceToHost));
+  for (int k = 0; k < OKV_K_COUNT; ++k) {
+    out->ms[k] = c->ms[k];
+    out->launches[k] = c->n_launch_kind[k];
+  }
+  out->fetched_blocks = (int64_t)h.fetched_blocks;
+  out->attended_slots = (int64_t)h.attended_slots;
+  return OKV_OK;
+}
+
+int64_t okv_launch_count(const okv_ctx* c) { return c ? c->launches : 0; }
+
+}  // extern "C"

@@ -1,0 +1,92 @@
+// Internal declarations of the okv CUDA library (sm_103a). Not part of the C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "../../include/okv.h"
+
+namespace okv {
+
+// Device error word: [0] = first error code (0 = none), [1..3] = details of that error.
+enum DeviceError : int32_t {
+  kErrNone = 0,
+  kErrBlockRange = 1,   // a block id outside [0, nb) of its unit
+  kErrSlotRange = 2,    // a slot outside [0, Kb)
+  kErrCapacity = 3,     // an append past the request's host capacity
+  kErrLength = 4,       // a context length outside [0, max_blocks * block_size]
+  kErrTimeout = 5,      // a bounded wait for an asynchronous copy gave up
+};
+
+// Geometry shared by host and kernels (passed by value).
+struct Geom {
+  int32_t L, Hq, Hkv, g, d, bs, kb, R, nb_max;
+  int32_t dtype;       // OKV_F32 / OKV_BF16
+  int32_t elem;        // bytes per element
+  int64_t block_bytes; // 2 * bs * d * elem: K and V of one block of one unit
+};
+
+// Per-layer views of the device state, all indexed [R][Hkv]...
+struct LayerState {
+  uint8_t* summ;        // [R][Hkv][nb_max][2][d] storage
+  uint8_t* pool;        // [R][Hkv][kb][2][bs][d] storage
+  int16_t* resident;    // [R][Hkv][nb_max] block -> slot or -1
+  int32_t* slot_block;  // [R][Hkv][kb] slot -> block or -1
+  int32_t* stamp;       // [R][Hkv][kb]
+  int32_t* sel_ids;     // [R][Hkv][kb]
+  float* sel_scores;    // [R][Hkv][kb]
+  int32_t* n_sel;       // [R][Hkv]
+  int32_t* fetch;       // [R][Hkv][kb][2] (block, slot)
+  int32_t* n_fetch;     // [R][Hkv]
+  int32_t* len;         // [R] tokens of each request at this layer
+};
+
+// Per-request device-side tables (shared by all layers).
+struct ReqTables {
+  const int32_t* active;    // [n_active] compact list of active request ids
+  const uint64_t* host_kv;  // [R] device address of the request's host KV buffer
+  const int32_t* cap_blocks;// [R]
+};
+
+struct Counters {
+  unsigned long long fetched_blocks;
+  unsigned long long attended_slots;
+};
+
+// ---- kernel launchers (defined in the k_*.cu files) --------------------------------------
+// Every launcher enqueues on `s` and returns cudaGetLastError().
+
+cudaError_t launch_summary_build(const Geom& G, int32_t layer_begin, int32_t layer_end,
+                                 int32_t req, uint64_t host_kv, int32_t cap_blocks,
+                                 int32_t n_tok, uint8_t* summ_base, int32_t* err,
+                                 cudaStream_t s);
+cudaError_t launch_append(const Geom& G, const LayerState& S, const ReqTables& T, int32_t n_active,
+                          int32_t layer, const void* k_new, const void* v_new, int32_t* err,
+                          cudaStream_t s);
+cudaError_t launch_reset_request(const Geom& G, int16_t* resident, int32_t* slot_block,
+                                 int32_t* stamp, int32_t* n_sel, int32_t* n_fetch, int32_t* len,
+                                 int32_t req, int32_t n_tok, uint64_t host_kv, int32_t cap,
+                                 uint64_t* host_kv_tab, int32_t* cap_tab, cudaStream_t s);
+cudaError_t launch_advance(const LayerState& S, const ReqTables& T, int32_t n_active, cudaStream_t s);
+cudaError_t launch_score_topk(const Geom& G, const LayerState& S, const ReqTables& T,
+                              int32_t n_active, int32_t max_nb, const void* draft,
+                              int32_t* err, cudaStream_t s);
+cudaError_t launch_select(const Geom& G, const LayerState& S, const ReqTables& T, int32_t n_active,
+                          int32_t cap_blocks, int32_t step, Counters* ctr, int32_t* err,
+                          cudaStream_t s);
+cudaError_t launch_gather(const Geom& G, const LayerState& S, const ReqTables& T, int32_t n_active,
+                          int32_t layer, int32_t max_fetch, int32_t* err, cudaStream_t s);
+// Attention: decides between the tensor-core path (bf16, d = 128, g <= 8) and the CUDA-core
+// path; `partials` is a workspace of at least attend_workspace_bytes() bytes.
+size_t attend_workspace_bytes(const Geom& G, int32_t n_active);
+cudaError_t launch_attend(const Geom& G, const LayerState& S, const ReqTables& T, int32_t n_active,
+                          int32_t layer, const void* q, void* out, const CUtensorMap* pool_map,
+                          void* partials, Counters* ctr, int32_t* err, cudaStream_t s,
+                          int* n_launches, int* used_split);
+bool attend_uses_tensor_cores(const Geom& G);
+
+}  // namespace okv

@@ -1,0 +1,254 @@
+"""Test rig: one okv context (CUDA library) and the CPU oracle over the same host KV bytes.
+
+Comparison rules (the method's tolerances):
+* block summaries, slot tables, stamps, fetch lists, pool bytes, lengths: exact;
+* selections: exact, except swaps between blocks whose oracle scores lie within
+  1e-6 * |s_K| of the K-th score s_K (binary32 scores summed in different orders may
+  order such near-ties differently); after an accepted selection the oracle's KV
+  selection step is re-synced to the GPU's selection so later state compares exactly;
+* attention: max abs error <= 1e-5 (binary32 storage) or 2e-2 (bfloat16 storage).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+import synth
+from sparse_kv_cache_draft_gb300 import BF16, F32, Config, Context, HostBuffer
+
+TIE_REL = 1e-6
+ATOL = {F32: 1e-5, BF16: 2e-2}
+
+
+def torch_dtype(dtype):
+    import torch
+    return torch.float32 if dtype == F32 else torch.bfloat16
+
+
+def to_device(a: np.ndarray, dtype):
+    import torch
+    a = np.ascontiguousarray(a)
+    t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if dtype == BF16 else torch.from_numpy(a)
+    return t.cuda()
+
+
+def out_to_f64(t, dtype) -> np.ndarray:
+    import torch
+    if dtype == BF16:
+        return t.float().cpu().numpy().astype(np.float64)
+    return t.cpu().numpy().astype(np.float64)
+
+
+class Rig:
+    def __init__(self, w: synth.Workload, *, contexts=None, capacity_tokens=None, n_alias=None,
+                 max_requests=None, active=None, layers_kept=None, n_threads=None):
+        self.w = w
+        B = w.batch
+        self.contexts = np.asarray(contexts if contexts is not None else w.contexts(), np.int32)
+        assert len(self.contexts) == B
+        cap_tok = capacity_tokens if capacity_tokens is not None else int(self.contexts.max()) + w.grow_per_step * w.steps
+        self.cap_blocks = -(-cap_tok // w.block_size)
+        self.R = max_requests or B
+        self.active = list(active) if active is not None else list(range(B))  # request ids used
+        assert len(self.active) == B and max(self.active) < self.R
+        self.n_alias = n_alias or B
+        self.keys = np.array([i % self.n_alias for i in range(B)], np.int32)
+        self.ids = np.array(self.active, np.int32)
+        nb_plant = -(-w.context // w.block_size)
+        self.plant_blocks = nb_plant
+        self.cfg = Config(layers=w.layers, q_heads=w.q_heads, kv_heads=w.kv_heads, head_dim=w.head_dim,
+                          block_size=w.block_size, budget_tokens=w.budget_tokens, max_requests=self.R,
+                          max_blocks_per_request=self.cap_blocks, fetch_cap=w.fetch_cap, dtype=w.dtype)
+        self.kb = self.cfg.slots
+        # host KV: one buffer per content key
+        self.bufs = {}
+        for i in range(B):
+            k = int(self.keys[i])
+            if k not in self.bufs:
+                hb = HostBuffer(self.cfg.host_bytes(self.cap_blocks))
+                n_fill = int(max(self.contexts[j] for j in range(B) if self.keys[j] == k))
+                synth.fill_kv(hb.ptr, w, k, 0, n_fill, self.cap_blocks, n_threads=n_threads,
+                              plant_blocks=nb_plant)
+                self.bufs[k] = hb
+        self.ctx = Context(self.cfg)
+        for i in range(B):
+            self.ctx.add_request(int(self.ids[i]), self.bufs[int(self.keys[i])].ptr, self.cap_blocks,
+                                 int(self.contexts[i]))
+        # the oracle sees request slot i of the batch (rows of the device arrays = request ids)
+        self.model = oracle.OracleModel(
+            layers=w.layers, q_heads=w.q_heads, kv_heads=w.kv_heads, head_dim=w.head_dim,
+            block_size=w.block_size, budget_tokens=w.budget_tokens, dtype=w.dtype,
+            req_ptrs=[self.bufs[int(k)].ptr for k in self.keys],
+            cap_blocks=[self.cap_blocks] * B, n_tok=self.contexts, n_threads=n_threads,
+            layers_kept=layers_kept)
+        self.sdt = np.float32 if w.dtype == F32 else np.uint16
+        self._summarised = set()  # (layer, batch index) whose oracle summaries are built
+
+    def _ensure_summaries(self, layer: int, requests=None) -> None:
+        reqs = range(self.w.batch) if requests is None else requests
+        todo = [i for i in reqs if (layer, i) not in self._summarised]
+        if todo:
+            self.model.build_summaries(layer, requests=todo)
+            self._summarised.update((layer, i) for i in todo)
+
+    # ---- inputs --------------------------------------------------------------------------------
+    def batch_queries(self, layer: int, step: int, kind: int) -> np.ndarray:
+        """[B][Hq][d] storage for the batch (row i = request ids[i])."""
+        return synth.queries(self.w, layer, step, kind, self.ids, self.keys, plant_blocks=self.plant_blocks)
+
+    def scatter(self, a: np.ndarray, rows_shape) -> np.ndarray:
+        """Place batch rows at their request ids in a [R]... array (other rows zero)."""
+        full = np.zeros((self.R,) + rows_shape, dtype=a.dtype)
+        full[self.ids] = a
+        return full
+
+    def device_rows(self, a: np.ndarray, rows_shape):
+        return to_device(self.scatter(a, rows_shape), self.w.dtype)
+
+    # ---- comparisons ---------------------------------------------------------------------------
+    def check_summaries(self, layer: int, requests=None) -> None:
+        reqs = range(self.w.batch) if requests is None else requests
+        self._ensure_summaries(layer, reqs)
+        for i in reqs:
+            gpu = self.ctx.read_summaries(layer, int(self.ids[i]))
+            nb = -(-int(self.model.n_tok[layer, i]) // self.w.block_size)
+            want = self.model.summ[layer][i][:, :nb]
+            assert np.array_equal(gpu[:, :nb], want), f"summaries differ: layer {layer} request {i}"
+
+    def check_selection(self, layer: int, requests=None):
+        """Compare the GPU selection with the oracle's (band rule); return the GPU selection as
+        (ids [B][Hkv][kb], counts [B][Hkv]) in batch order, for re-syncing the oracle."""
+        counts, ids, scores = self.ctx.read_selection(layer)
+        reqs = range(self.w.batch) if requests is None else requests
+        B, H, kb = self.w.batch, self.w.kv_heads, self.kb
+        g_ids = np.full((B, H, kb), -1, np.int32)
+        g_cnt = np.zeros((B, H), np.int32)
+        n_swaps = 0
+        for i in reqs:
+            r = int(self.ids[i])
+            nb = -(-int(self.model.n_tok[layer, i]) // self.w.block_size)
+            for h in range(H):
+                n = min(kb, nb)
+                assert counts[r, h] == n, (layer, i, h, counts[r, h], n)
+                gsel = ids[r, h, :n]
+                osel = self.model.sel_ids[layer][i, h, :n]
+                osc = self.model.scores[layer][i, h, :nb]
+                assert len(set(gsel.tolist())) == n and gsel.min() >= 0 and gsel.max() < nb
+                # GPU order: its own scores non-increasing, ties by block id
+                gs = scores[r, h, :n]
+                assert np.all((gs[:-1] > gs[1:]) | ((gs[:-1] == gs[1:]) & (gsel[:-1] < gsel[1:]))), (layer, i, h)
+                # GPU scores agree with the oracle's within binary32 summation error
+                assert np.allclose(gs, osc[gsel], rtol=2e-6, atol=1e-6 * max(1.0, float(np.abs(osc).max()))), \
+                    (layer, i, h, float(np.abs(gs - osc[gsel]).max()))
+                if not np.array_equal(np.sort(gsel), np.sort(osel)):
+                    sK = float(osc[osel[-1]])
+                    band = set(np.nonzero(np.abs(osc.astype(np.float64) - sK) <= TIE_REL * abs(sK))[0].tolist())
+                    diff = set(gsel.tolist()) ^ set(osel.tolist())
+                    assert diff <= band, f"selection differs outside the tie band: layer {layer} req {i} head {h}: {sorted(diff - band)}"
+                    n_swaps += 1
+                g_ids[i, h, :n] = gsel
+                g_cnt[i, h] = n
+        return (g_ids, g_cnt), n_swaps
+
+    def check_tables(self, layer: int, requests=None) -> None:
+        sb, st = self.ctx.read_slot_table(layer)
+        counts, entries = self.ctx.read_fetch_list(layer)
+        reqs = range(self.w.batch) if requests is None else requests
+        for i in reqs:
+            r = int(self.ids[i])
+            assert np.array_equal(sb[r], self.model.slot_block[layer][i]), f"slot table: layer {layer} req {i}"
+            occ = sb[r] >= 0
+            assert np.array_equal(st[r][occ], self.model.stamp[layer][i][occ]), f"stamps: layer {layer} req {i}"
+            assert np.array_equal(counts[r], self.model.n_fetch[layer][i]), f"fetch counts: layer {layer} req {i}"
+            for h in range(self.w.kv_heads):
+                n = int(counts[r, h])
+                assert np.array_equal(entries[r, h, :n], self.model.fetch[layer][i, h, :n]), \
+                    f"fetch list: layer {layer} req {i} head {h}"
+
+    def check_pool(self, layer: int, requests=None, heads=None) -> None:
+        sb, _ = self.ctx.read_slot_table(layer)
+        reqs = range(self.w.batch) if requests is None else requests
+        bs = self.w.block_size
+        for i in reqs:
+            r = int(self.ids[i])
+            n_tok = int(self.model.n_tok[layer, i])
+            for h in (range(self.w.kv_heads) if heads is None else heads):
+                pool = self.ctx.read_pool(layer, r, h)
+                host = self.model.host_unit(layer, i, h)
+                for s in range(self.kb):
+                    b = int(sb[r, h, s])
+                    if b < 0:
+                        continue
+                    nv = min(bs, n_tok - b * bs)
+                    assert np.array_equal(pool[s, :, :nv], host[b, :, :nv]), \
+                        f"pool slot differs from host block: layer {layer} req {i} head {h} slot {s} block {b}"
+
+    def check_attention(self, layer: int, q: np.ndarray, out_dev, requests=None) -> float:
+        """q: [B][Hq][d] storage (batch order); out_dev: device [R][Hq][d]."""
+        got = out_to_f64(out_dev, self.w.dtype)[self.ids]
+        want = self.model.attend(layer, q, requests=requests)
+        reqs = list(range(self.w.batch)) if requests is None else list(requests)
+        err = float(np.abs(got[reqs] - want[reqs]).max()) if reqs else 0.0
+        assert err <= ATOL[self.w.dtype], f"attention max abs error {err} at layer {layer}"
+        return err
+
+    # ---- one staging + attention round ---------------------------------------------------------
+    def stage(self, layer: int, step: int, cap: float, draft_step: int | None = None, requests=None,
+              check_pool=True):
+        import torch
+        ds = step - 1 if draft_step is None else draft_step
+        draft = self.batch_queries(layer, ds, 1)
+        self.ctx.stage(layer, self.device_rows(draft, (self.w.q_heads, self.w.head_dim)), step, cap)
+        torch.cuda.synchronize()
+        assert self.ctx.sync(60_000) == 0
+        self._ensure_summaries(layer, requests)
+        self.model.score_topk(layer, draft, requests=requests)
+        gsel, swaps = self.check_selection(layer, requests=requests)
+        C = oracle.fetch_cap_blocks(cap, self.kb)
+        self.model.select(layer, C, step, sel_override=gsel, requests=requests)
+        self.check_tables(layer, requests=requests)
+        if check_pool:
+            self.check_pool(layer, requests=requests)
+        return swaps
+
+    def attend(self, layer: int, step: int, requests=None) -> float:
+        import torch
+        q = self.batch_queries(layer, step, 0)
+        out = torch.zeros((self.R, self.w.q_heads, self.w.head_dim), dtype=torch_dtype(self.w.dtype),
+                          device="cuda")
+        self.ctx.attend(layer, self.device_rows(q, (self.w.q_heads, self.w.head_dim)), out)
+        torch.cuda.synchronize()
+        return self.check_attention(layer, q, out, requests=requests)
+
+    def run_steps(self, n_steps: int, cap: float, bootstrap_cap: float = 1.0, layers=None,
+                  requests=None, check_pool=True, append=False):
+        """Bootstrap staging (draft of step -1, stamp 0), then n_steps decode steps: for each
+        layer, [append the step's token,] attend(q_t), stage(draft_t) with stamp t + 1."""
+        import torch
+        layers = range(self.w.layers) if layers is None else layers
+        errs, swaps = [], 0
+        for layer in layers:
+            swaps += self.stage(layer, 0, bootstrap_cap, draft_step=-1, requests=requests, check_pool=check_pool)
+        for t in range(n_steps):
+            for layer in layers:
+                if append:
+                    self.append(layer)
+                errs.append(self.attend(layer, t, requests=requests))
+                swaps += self.stage(layer, t + 1, cap, draft_step=t, requests=requests, check_pool=check_pool)
+        return errs, swaps
+
+    def append(self, layer: int) -> None:
+        """Append each request's next token (the generator's token at its position)."""
+        import torch
+        pos = self.model.n_tok[layer].copy()
+        self._ensure_summaries(layer)
+        k, v = synth.token_kv(self.w, layer, self.keys, pos, plant_blocks=self.plant_blocks)
+        shp = (self.w.kv_heads, self.w.head_dim)
+        self.ctx.append(layer, self.device_rows(k, shp), self.device_rows(v, shp))
+        torch.cuda.synchronize()
+        self.model.append(layer, k, v)
+
+    def close(self):
+        self.ctx.close()
+        for b in self.bufs.values():
+            b.free()

@@ -1,0 +1,178 @@
+"""CUDA path vs the CPU oracle, through the C ABI (needs a GB300)."""
+import numpy as np
+import pytest
+
+import synth
+from okv_harness import ATOL, Rig
+from sparse_kv_cache_draft_gb300 import BF16, F32, OkvError
+
+pytestmark = pytest.mark.gpu
+
+QWEN = synth.WORKLOADS["qwen3_8b_16k_b128"]
+
+
+def test_tiny_single_step():
+    """Tiny config: batch 2, GQA 8/2, d 64, 4096 tokens, budget 512, cap 1.0, fp32."""
+    w = synth.WORKLOADS["tiny"]
+    rig = Rig(w)
+    try:
+        rig.check_summaries(0)
+        assert rig.attend(0, 0) == 0.0  # empty pool: zeros on both sides
+        rig.stage(0, 0, 1.0, draft_step=-1)
+        err = rig.attend(0, 0)
+        assert err <= ATOL[F32]
+        sb, _ = rig.ctx.read_slot_table(0)
+        counts, ids, _ = rig.ctx.read_selection(0)
+        for r in range(w.batch):
+            for h in range(w.kv_heads):
+                # fetch cap 1.0: the resident set equals the selection
+                assert set(sb[r, h][sb[r, h] >= 0].tolist()) == set(ids[r, h, :counts[r, h]].tolist())
+    finally:
+        rig.close()
+
+
+def test_qwen_shapes_multistep_cap005():
+    """Qwen3-8B attention shapes (32/8 heads, d 128, 16K, bf16), 2 layers x 3 requests, state carried
+    over a bootstrap and 4 decode steps at fetch cap 0.05 (C = 6)."""
+    w = QWEN.scaled(layers=2, batch=3)
+    rig = Rig(w)
+    try:
+        rig.check_summaries(0)
+        rig.check_summaries(1)
+        errs, _ = rig.run_steps(4, 0.05)
+        assert max(errs) <= ATOL[BF16]
+        counts, _ = rig.ctx.read_fetch_list(1)
+        assert counts[:3].max() <= 6
+    finally:
+        rig.close()
+
+
+def test_ragged_contexts_and_inactive_rows():
+    """Contexts 1, 17, 300, 2048 and 5000 tokens (1 to 313 blocks, partial tails, fewer blocks
+    than slots) on request ids 0, 2, 3, 5, 7 of 8."""
+    w = QWEN.scaled(layers=1, batch=5)
+    rig = Rig(w, contexts=[1, 17, 300, 2048, 5000], max_requests=8, active=[0, 2, 3, 5, 7])
+    try:
+        rig.check_summaries(0)
+        errs, _ = rig.run_steps(3, 0.05)
+        assert max(errs) <= ATOL[BF16]
+        sb, _ = rig.ctx.read_slot_table(0)
+        # budget covers the context for the first four: after the bootstrap every block is resident
+        for i, n_tok in enumerate([1, 17, 300, 2048]):
+            nb = -(-n_tok // 16)
+            for h in range(w.kv_heads):
+                assert sorted(sb[rig.ids[i], h][sb[rig.ids[i], h] >= 0].tolist()) == list(range(nb))
+    finally:
+        rig.close()
+
+
+def test_many_units_unsplit_attention():
+    """160 requests x 8 KV heads = 1280 units: one CTA per unit, no split combine."""
+    w = QWEN.scaled(layers=1, batch=160, context=2048 + 40)
+    rig = Rig(w, n_alias=4)
+    try:
+        sample = [0, 1, 77, 159]
+        errs, _ = rig.run_steps(2, 0.05, requests=sample, check_pool=False)
+        assert max(errs) <= ATOL[BF16]
+        rig.check_pool(0, requests=sample)
+    finally:
+        rig.close()
+
+
+def test_gqa8_32b_class_shape():
+    """32B-class GQA shape: 64 query / 8 KV heads (group 8), d 128, 32K context."""
+    w = synth.WORKLOADS["gqa32b_32k_b32"].scaled(layers=1, batch=2)
+    rig = Rig(w)
+    try:
+        errs, _ = rig.run_steps(3, 0.05)
+        assert max(errs) <= ATOL[BF16]
+    finally:
+        rig.close()
+
+
+@pytest.mark.parametrize("dtype,d,g", [(BF16, 64, 4), (F32, 128, 4), (F32, 64, 8)])
+def test_cuda_core_path_shapes(dtype, d, g):
+    """Shapes served by the CUDA-core attention kernel."""
+    w = QWEN.scaled(layers=1, batch=2, dtype=dtype, head_dim=d, q_heads=8 * g, kv_heads=8,
+                    context=3000, budget_tokens=512)
+    rig = Rig(w)
+    try:
+        errs, _ = rig.run_steps(2, 0.25)
+        assert max(errs) <= ATOL[dtype]
+    finally:
+        rig.close()
+
+
+def test_append_growing_contexts():
+    """Mixed lengths growing one token per step across block boundaries: host writes, resident
+    tail-slot writes and min/max summary updates."""
+    w = synth.WORKLOADS["qwen3_8b_mixed_b64"].scaled(layers=2, batch=3, steps=40)
+    rig = Rig(w, contexts=[1000, 2047, 4095])
+    try:
+        errs, _ = rig.run_steps(40, 0.05, append=True)
+        assert max(errs) <= ATOL[BF16]
+        for layer in range(2):
+            rig.check_summaries(layer)
+            lens = rig.ctx.read_lengths(layer)
+            assert lens[:3].tolist() == [1040, 2087, 4135]
+    finally:
+        rig.close()
+
+
+def test_shared_host_buffers():
+    """Requests registered on the same host buffer share summaries; appending to them is refused."""
+    w = QWEN.scaled(layers=2, batch=4, context=4096)
+    rig = Rig(w, n_alias=2)
+    try:
+        for layer in range(2):
+            rig.check_summaries(layer)
+        errs, _ = rig.run_steps(2, 0.05)
+        assert max(errs) <= ATOL[BF16]
+        import torch
+        z = torch.zeros((4, 8, 128), dtype=torch.bfloat16, device="cuda")
+        with pytest.raises(OkvError):
+            rig.ctx.append(0, z, z)
+    finally:
+        rig.close()
+
+
+def test_api_errors():
+    import torch
+    from sparse_kv_cache_draft_gb300 import Config, Context, HostBuffer, binding
+    with pytest.raises(OkvError):
+        Context(Config(1, 6, 4, 128, 16, 2048, 2, 64))  # q heads not a multiple of kv heads
+    with pytest.raises(OkvError):
+        Context(Config(1, 8, 2, 100, 16, 2048, 2, 64))  # head_dim not a multiple of 32
+    cfg = Config(1, 8, 2, 64, 16, 512, 2, 8, 1.0, F32)
+    ctx = Context(cfg)
+    hb = HostBuffer(cfg.host_bytes(8))
+    try:
+        with pytest.raises(OkvError) as e:
+            ctx.add_request(2, hb.ptr, 8, 16)
+        assert e.value.status == binding.EINVAL
+        with pytest.raises(OkvError):
+            ctx.add_request(0, hb.ptr, 8, 8 * 16 + 1)  # more tokens than capacity
+        unpinned = np.zeros(cfg.host_bytes(8) // 4, np.float32)
+        with pytest.raises(OkvError):
+            ctx.add_request(0, unpinned.ctypes.data, 8, 16)
+        ctx.add_request(0, hb.ptr, 8, 8 * 16)
+        with pytest.raises(OkvError) as e:
+            ctx.add_request(0, hb.ptr, 8, 16)
+        assert e.value.status == binding.ESTATE
+        q = torch.zeros((2, 8, 64), device="cuda")
+        with pytest.raises(OkvError):
+            ctx.attend(1, q, q)  # layer out of range
+        with pytest.raises(OkvError):
+            ctx.stage(0, q, 0, 1.5)  # cap outside (0, 1]
+        kv = torch.zeros((2, 2, 64), device="cuda")
+        with pytest.raises(OkvError):
+            ctx.append(0, kv, kv)  # request 0 is full
+        with pytest.raises(ValueError):
+            ctx.attend(0, q.half(), q)  # wrong dtype is refused before the call
+        ctx.remove_request(0)
+        with pytest.raises(OkvError):
+            ctx.remove_request(0)
+        assert ctx.sync(1000) == 0
+    finally:
+        ctx.close()
+        hb.free()
