@@ -54,6 +54,9 @@ def parse_args():
     p.add_argument("--alias", type=int, default=16, help="distinct host KV buffers the batch aliases")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--threads", type=int, default=0)
+    p.add_argument("--batch", type=int, default=0, help="override the batch (smaller profiling cases)")
+    p.add_argument("--layers", type=int, default=0, help="override the layer count (smaller profiling cases)")
+    p.add_argument("--baseline-layers", type=int, default=6, help="layers in the cpu_baseline sample")
     return p.parse_args()
 
 
@@ -174,12 +177,16 @@ def pinned_h2d_gbs(nbytes=1 << 30, reps=5) -> float:
 # ---- workload setup ----------------------------------------------------------------------------
 
 class Workload:
-    def __init__(self, alias: int, threads: int):
+    def __init__(self, alias: int, threads: int, batch: int = 0, layers: int = 0):
         import numpy as np
         import synth
         self.np = np
         self.synth = synth
         self.w = synth.WORKLOADS[WORKLOAD]
+        if batch:
+            self.w = self.w.scaled(batch=batch)
+        if layers:
+            self.w = self.w.scaled(layers=layers)
         w = self.w
         self.B, self.L, self.Hq, self.Hkv, self.d = w.batch, w.layers, w.q_heads, w.kv_heads, w.head_dim
         self.n_tok = w.context
@@ -213,7 +220,8 @@ class Workload:
 
     def config_json(self):
         w = self.w
-        return {"workload": WORKLOAD, "model_shapes": "Qwen3-8B attention", "batch": self.B, "seq_len": self.n_tok,
+        return {"workload": WORKLOAD if (self.B, self.L) == (128, 36) else f"{WORKLOAD} (batch {self.B}, {self.L} layers)",
+                "model_shapes": "Qwen3-8B attention", "batch": self.B, "seq_len": self.n_tok,
                 "layers": self.L, "q_heads": self.Hq, "kv_heads": self.Hkv, "head_dim": self.d,
                 "block_size": w.block_size, "budget_tokens": w.budget_tokens, "fetch_cap": w.fetch_cap,
                 "host_kv_buffers": self.alias, "parallelism": "replicas",
@@ -276,7 +284,7 @@ def run_okv(args, dist: Dist):
 
     load_library()
     torch.cuda.set_device(dist.local)
-    wl = Workload(args.alias, args.threads)
+    wl = Workload(args.alias, args.threads, args.batch, args.layers)
     cfg = wl.config()
     B, L, Hq, d = wl.B, wl.L, wl.Hq, wl.d
     K, W = args.steps, args.warmup
@@ -411,7 +419,7 @@ def run_okv(args, dist: Dist):
     }
     if not args.no_cpu_baseline and dist.rank == 0:
         t0 = time.time()
-        res["cpu_baseline"] = cpu_baseline(wl, bufs)
+        res["cpu_baseline"] = cpu_baseline(wl, bufs, min(args.baseline_layers, wl.L))
         log(f"cpu baseline sample took {time.time() - t0:.1f}s")
     ctx.close()
     for b in bufs:
@@ -422,9 +430,9 @@ def run_okv(args, dist: Dist):
 def run_reference(args, dist: Dist):
     if dist.rank != 0:
         return None
-    wl = Workload(args.alias, args.threads)
+    wl = Workload(args.alias, args.threads, args.batch, args.layers)
     bufs = wl.host_kv()
-    n_layers_used = 4
+    n_layers_used = min(4, wl.L)
     t = OracleTimer(wl, bufs, range(n_layers_used))
     for l in range(n_layers_used):
         t.prepare(l)

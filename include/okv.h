@@ -146,7 +146,8 @@ OKV_API okv_status okv_join(okv_ctx* ctx, void* stream);
 OKV_API okv_status okv_sync(okv_ctx* ctx, int64_t timeout_ms);
 
 /* ---- inspection: synchronise the internal streams, then copy to caller-owned host arrays.
- * The caller must first synchronise any stream it passed to okv_attend / okv_append. ---- */
+ * The caller must first synchronise any stream it passed to okv_attend / okv_append /
+ * okv_stage. ---- */
 
 /* Summaries of one request: out [kv_heads][max_blocks_per_request][2][head_dim] storage. */
 OKV_API okv_status okv_read_summaries(okv_ctx* ctx, int32_t layer, int32_t req, void* out);

@@ -5,6 +5,8 @@
 // forward pass. Here the SMs read the host buffer directly over the host link (the buffer is
 // device-mapped), one warp per block: every lane issues all of its 16-byte loads of the block
 // before storing, so a warp keeps a whole block in flight.
+#include <stdlib.h>
+
 #include "okv_internal.h"
 
 namespace okv {
@@ -21,38 +23,44 @@ __device__ __forceinline__ void record_error(int32_t* err, int32_t code, int32_t
   }
 }
 
-// grid (units, ceil(max_fetch / kGatherWarps)); warp w copies fetch entry y * warps + w.
+// Persistent grid: warp w of the grid copies work items w, w + nwarps, ... where item i is
+// entry i % cmax of active unit i / cmax (items past the unit's fetch count are skipped).
 template <int kVecPerLane>
 __global__ void __launch_bounds__(kGatherWarps * 32)
-gather_kernel(Geom G, LayerState S, ReqTables RT, int32_t layer, int32_t* err) {
-  const int32_t a = blockIdx.x / G.Hkv, h = blockIdx.x % G.Hkv;
-  const int32_t r = RT.active[a];
-  const int64_t unit = (int64_t)r * G.Hkv + h;
-  const int32_t e = blockIdx.y * kGatherWarps + (threadIdx.x >> 5);
-  if (e >= S.n_fetch[unit]) return;
+gather_kernel(Geom G, LayerState S, ReqTables RT, int32_t layer, int32_t n_units, int32_t cmax,
+              int32_t* err) {
   const int lane = threadIdx.x & 31;
-  const int32_t b = S.fetch[(unit * G.kb + e) * 2 + 0];
-  const int32_t s = S.fetch[(unit * G.kb + e) * 2 + 1];
-  const int32_t cap = RT.cap_blocks[r];
-  if (b < 0 || b >= cap || s < 0 || s >= G.kb) {
-    if (lane == 0) record_error(err, b < 0 || b >= cap ? kErrBlockRange : kErrSlotRange, layer, r, e);
-    return;
-  }
-  const uint4* src = reinterpret_cast<const uint4*>(
-      RT.host_kv[r] + (((int64_t)layer * G.Hkv + h) * cap + b) * G.block_bytes);
-  uint4* dst = reinterpret_cast<uint4*>(S.pool + (unit * G.kb + s) * G.block_bytes);
+  const int64_t nw = (int64_t)gridDim.x * kGatherWarps;
+  const int64_t total = (int64_t)n_units * cmax;
   const int32_t nvec = (int32_t)(G.block_bytes / 16);
-  for (int32_t base = 0; base < nvec; base += 32 * kVecPerLane) {
-    uint4 x[kVecPerLane];
-#pragma unroll
-    for (int i = 0; i < kVecPerLane; ++i) {
-      const int32_t v = base + i * 32 + lane;
-      if (v < nvec) x[i] = __ldcs(src + v);
+  for (int64_t it = (int64_t)blockIdx.x * kGatherWarps + (threadIdx.x >> 5); it < total; it += nw) {
+    const int32_t ua = (int32_t)(it / cmax), e = (int32_t)(it % cmax);
+    const int32_t a = ua / G.Hkv, h = ua % G.Hkv;
+    const int32_t r = RT.active[a];
+    const int64_t unit = (int64_t)r * G.Hkv + h;
+    if (e >= S.n_fetch[unit]) continue;
+    const int32_t b = S.fetch[(unit * G.kb + e) * 2 + 0];
+    const int32_t s = S.fetch[(unit * G.kb + e) * 2 + 1];
+    const int32_t cap = RT.cap_blocks[r];
+    if (b < 0 || b >= cap || s < 0 || s >= G.kb) {
+      if (lane == 0) record_error(err, b < 0 || b >= cap ? kErrBlockRange : kErrSlotRange, layer, r, e);
+      continue;
     }
+    const uint4* src = reinterpret_cast<const uint4*>(
+        RT.host_kv[r] + (((int64_t)layer * G.Hkv + h) * cap + b) * G.block_bytes);
+    uint4* dst = reinterpret_cast<uint4*>(S.pool + (unit * G.kb + s) * G.block_bytes);
+    for (int32_t base = 0; base < nvec; base += 32 * kVecPerLane) {
+      uint4 x[kVecPerLane];
 #pragma unroll
-    for (int i = 0; i < kVecPerLane; ++i) {
-      const int32_t v = base + i * 32 + lane;
-      if (v < nvec) __stcs(dst + v, x[i]);
+      for (int i = 0; i < kVecPerLane; ++i) {
+        const int32_t v = base + i * 32 + lane;
+        if (v < nvec) x[i] = __ldcs(src + v);
+      }
+#pragma unroll
+      for (int i = 0; i < kVecPerLane; ++i) {
+        const int32_t v = base + i * 32 + lane;
+        if (v < nvec) __stcs(dst + v, x[i]);
+      }
     }
   }
 }
@@ -62,8 +70,20 @@ gather_kernel(Geom G, LayerState S, ReqTables RT, int32_t layer, int32_t* err) {
 cudaError_t launch_gather(const Geom& G, const LayerState& S, const ReqTables& T, int32_t n_active,
                           int32_t layer, int32_t max_fetch, int32_t* err, cudaStream_t s) {
   if (n_active <= 0 || max_fetch <= 0) return cudaSuccess;
-  dim3 grid(n_active * G.Hkv, (max_fetch + kGatherWarps - 1) / kGatherWarps);
-  gather_kernel<16><<<grid, kGatherWarps * 32, 0, s>>>(G, S, T, layer, err);
+  static int ctas = [] {
+    int n = 0;
+    if (const char* e = getenv("OKV_GATHER_CTAS")) n = atoi(e);
+    if (n <= 0) {
+      int dev = 0, sms = 152;
+      if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      n = sms;
+    }
+    return n;
+  }();
+  const int64_t items = (int64_t)n_active * G.Hkv * max_fetch;
+  const int64_t want = (items + kGatherWarps - 1) / kGatherWarps;
+  const int grid = (int)(want < ctas ? want : ctas);
+  gather_kernel<16><<<grid, kGatherWarps * 32, 0, s>>>(G, S, T, layer, n_active * G.Hkv, max_fetch, err);
   return cudaGetLastError();
 }
 

@@ -34,35 +34,57 @@ __device__ __forceinline__ float from_orderable(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-// ---- score + top-K ------------------------------------------------------------------------
+// ---- block-wide helpers -------------------------------------------------------------------
+
+// Exclusive prefix count of `flag` over the thread order of one pass of the block (index
+// base + threadIdx.x); returns this thread's rank and sets *total to the pass's count.
+__device__ __forceinline__ int32_t block_rank(bool flag, int32_t* scratch, int32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const unsigned ballot = __ballot_sync(0xffffffffu, flag);
+  if (lane == 0) scratch[warp] = __popc(ballot);
+  __syncthreads();
+  int32_t before = 0, all = 0;
+  for (int w = 0; w < nwarps; ++w) {
+    if (w < warp) before += scratch[w];
+    all += scratch[w];
+  }
+  __syncthreads();
+  *total = all;
+  return before + __popc(ballot & ((1u << lane) - 1u));
+}
+
+// ---- block scores -------------------------------------------------------------------------
 //
 // Score of block b for KV head h: sum over the g query heads of the group of
 // sum_c max(q_c kmin_c, q_c kmax_c) = sum_c (P_c kmax_c + N_c kmin_c), P_c (N_c) being the sum
-// of the group's positive (negative) query coordinates. One CTA per unit; each warp reads one
-// 16-byte vector per lane of a block's [kmin | kmax] record (2d elements), multiplies by the
-// matching N or P coefficient and reduces across the warp. Keys (orderable score, ~block id)
-// then go through a bitonic sort in shared memory, descending: score desc, block id asc.
+// of the group's positive (negative) query coordinates. One CTA scores kScoreChunk blocks of
+// one unit; each warp reads one 16-byte vector per lane of a block's [kmin | kmax] record (2d
+// elements), multiplies by the matching N or P coefficient and reduces across the warp. The
+// order-preserving 32-bit image of each binary32 score goes to `ord`.
+constexpr int kScoreChunk = 128;
+
 template <typename T>
 __global__ void __launch_bounds__(kScoreThreads)
-score_topk_kernel(Geom G, LayerState S, ReqTables RT, int32_t np2, const T* __restrict__ draft,
-                  int32_t* err) {
+score_kernel(Geom G, LayerState S, ReqTables RT, int32_t chunks, const T* __restrict__ draft,
+             uint32_t* __restrict__ ord_out, int32_t* err) {
   constexpr int V = 16 / sizeof(T);
   extern __shared__ __align__(16) uint8_t smem[];
-  float* coef = reinterpret_cast<float*>(smem);                               // [2d]
-  unsigned long long* keys = reinterpret_cast<unsigned long long*>(coef + 2 * G.d);  // [np2]
-
-  const int32_t a = blockIdx.x / G.Hkv, h = blockIdx.x % G.Hkv;
+  float* coef = reinterpret_cast<float*>(smem);  // [2d]
+  const int32_t ua = blockIdx.x / chunks, chunk = blockIdx.x % chunks;
+  const int32_t a = ua / G.Hkv, h = ua % G.Hkv;
   const int32_t r = RT.active[a];
   const int64_t unit = (int64_t)r * G.Hkv + h;
   const int32_t len = S.len[r];
   const int32_t nb = (len + G.bs - 1) / G.bs;
-  if (nb > np2 || nb > G.nb_max) {
-    if (threadIdx.x == 0) record_error(err, kErrLength, -1, r, len);
+  const int32_t b_lo = chunk * kScoreChunk;
+  if (len < 0 || nb > G.nb_max) {
+    if (threadIdx.x == 0 && chunk == 0) record_error(err, kErrLength, -1, r, len);
     return;
   }
-
-  // P_c (max part, multiplies kmax) and N_c (min part, multiplies kmin), group heads in order
-  for (int32_t c = threadIdx.x; c < G.d; c += blockDim.x) {
+  if (b_lo >= nb) return;
+  const int32_t b_hi = min(nb, b_lo + kScoreChunk);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  for (int32_t c = tid; c < G.d; c += blockDim.x) {
     float p = 0.f, n = 0.f;
     for (int32_t j = 0; j < G.g; ++j) {
       const float x = to_f(draft[((int64_t)r * G.Hq + h * G.g + j) * G.d + c]);
@@ -73,12 +95,11 @@ score_topk_kernel(Geom G, LayerState S, ReqTables RT, int32_t np2, const T* __re
     coef[G.d + c] = p;
   }
   __syncthreads();
-
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const int32_t nvec = 2 * G.d / V;  // 16-byte vectors per summary record
   const T* summ = reinterpret_cast<const T*>(S.summ) + unit * G.nb_max * 2 * G.d;
+  uint32_t* ord = ord_out + unit * G.nb_max;
   constexpr int U = 4;  // blocks in flight per warp
-  for (int32_t b0 = warp * U; b0 < nb; b0 += nwarps * U) {
+  for (int32_t b0 = b_lo + warp * U; b0 < b_hi; b0 += nwarps * U) {
     float part[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) part[u] = 0.f;
@@ -90,10 +111,8 @@ score_topk_kernel(Geom G, LayerState S, ReqTables RT, int32_t np2, const T* __re
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int32_t b = b0 + u;
-        if (b < nb)
-          x[u].u4 = __ldcs(reinterpret_cast<const uint4*>(summ + (int64_t)b * 2 * G.d) + v);
-        else
-          x[u].u4 = make_uint4(0, 0, 0, 0);
+        x[u].u4 = b < b_hi ? __ldcs(reinterpret_cast<const uint4*>(summ + (int64_t)b * 2 * G.d) + v)
+                           : make_uint4(0, 0, 0, 0);
       }
       const float* cf = coef + v * V;
 #pragma unroll
@@ -110,27 +129,128 @@ score_topk_kernel(Geom G, LayerState S, ReqTables RT, int32_t np2, const T* __re
       for (int o = 16; o > 0; o >>= 1) part[u] += __shfl_xor_sync(0xffffffffu, part[u], o);
     }
     if (lane < U) {
-      float s = part[0];
+      float sc = part[0];
 #pragma unroll
       for (int u = 1; u < U; ++u)
-        if (lane == u) s = part[u];
-      const int32_t b = b0 + lane;
-      if (b < nb)
-        keys[b] = ((unsigned long long)orderable(s) << 32) | (unsigned long long)(~(uint32_t)b);
+        if (lane == u) sc = part[u];
+      if (b0 + lane < b_hi) ord[b0 + lane] = orderable(sc);
     }
   }
-  for (int32_t i = nb + threadIdx.x; i < np2; i += blockDim.x) keys[i] = 0ull;  // below any score
+}
+
+// ---- top-K and diff / admit / evict, one CTA per unit -------------------------------------
+//
+// Top-K: a radix select over the order-preserving 32-bit score images finds the K-th largest
+// score T; blocks above T are selected, and of the blocks equal to T the lowest ids fill the
+// rest. The K selected (score, ~id) keys are then sorted, descending.
+//
+// Diff / admit / evict: hits (selected and resident) keep their slot and get stamp = step;
+// misses are ranked in selection order and the first min(C, #misses) are admitted; targets are
+// free slots by ascending slot, then unselected resident blocks by (stamp asc, block id asc);
+// each admitted block takes the target of its rank, the evicted block leaves the resident map,
+// and (block, slot) is appended to the fetch list.
+__global__ void __launch_bounds__(kScoreThreads)
+select_kernel(Geom G, LayerState S, ReqTables RT, int32_t nb_cap, int32_t kp2,
+              const uint32_t* __restrict__ ord_in, int32_t cap_blocks, int32_t step, Counters* ctr,
+              int32_t* err) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem);  // [kp2] selected keys
+  unsigned long long* tkey = keys + kp2;                                   // [kb] eviction order
+  uint32_t* ord = reinterpret_cast<uint32_t*>(tkey + G.kb);                // [nb_cap] score images
+  uint32_t* hist = ord + nb_cap;                                           // [256]
+  int32_t* sb = reinterpret_cast<int32_t*>(hist + 256);                    // [kb] slot -> block
+  int32_t* st = sb + G.kb;                                                 // [kb] stamps
+  int32_t* hit = st + G.kb;                                                // [kb]
+  int32_t* target = hit + G.kb;                                            // [kb]
+  int32_t* selid = target + G.kb;                                          // [kb] selection, in order
+  int32_t* missrank = selid + G.kb;                                        // [kb] rank of a miss or -1
+  int32_t* scratch = missrank + G.kb;                                      // [32 + 4]
+
+  const int32_t a = blockIdx.x / G.Hkv, h = blockIdx.x % G.Hkv;
+  const int32_t r = RT.active[a];
+  const int64_t unit = (int64_t)r * G.Hkv + h;
+  const int32_t len = S.len[r];
+  const int32_t nb = (len + G.bs - 1) / G.bs;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (nb > nb_cap || nb > G.nb_max || len < 0) {
+    if (tid == 0) record_error(err, kErrLength, -1, r, len);
+    return;
+  }
+  for (int32_t b = tid; b < nb; b += blockDim.x) ord[b] = ord_in[unit * G.nb_max + b];
   __syncthreads();
 
-  // bitonic sort, descending
-  for (int32_t k = 2; k <= np2; k <<= 1) {
+  // ---- top-K: radix select of the K-th largest score image ----
+  const int32_t K = nb < G.kb ? nb : G.kb;
+  uint32_t prefix = 0, mask = 0;
+  int32_t krem = K;
+  if (K < nb) {
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      for (int32_t i = tid; i < 256; i += blockDim.x) hist[i] = 0;
+      __syncthreads();
+      for (int32_t b = tid; b < nb; b += blockDim.x) {
+        const uint32_t u = ord[b];
+        if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
+      }
+      __syncthreads();
+      if (warp == 0) {
+        // lane l owns digits 255 - 8l .. 248 - 8l (high to low)
+        uint32_t cnt[8], own = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          cnt[i] = hist[255 - 8 * lane - i];
+          own += cnt[i];
+        }
+        uint32_t incl = own;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const uint32_t excl = incl - own;
+        if (excl < (uint32_t)krem && (uint32_t)krem <= incl) {
+          uint32_t run = excl;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (run + cnt[i] >= (uint32_t)krem) {
+              scratch[32] = 255 - 8 * lane - i;
+              scratch[33] = krem - (int32_t)run;
+              break;
+            }
+            run += cnt[i];
+          }
+        }
+      }
+      __syncthreads();
+      prefix |= (uint32_t)scratch[32] << shift;
+      mask |= 255u << shift;
+      krem = scratch[33];
+      __syncthreads();
+    }
+  }
+  // prefix = K-th largest image T (K < nb); krem = how many blocks equal to T are taken
+  int32_t base_eq = 0, base_sel = 0;
+  for (int32_t b0 = 0; b0 < nb; b0 += blockDim.x) {
+    const int32_t b = b0 + tid;
+    const uint32_t u = b < nb ? ord[b] : 0u;
+    const bool eq = K < nb && b < nb && u == prefix;
+    int32_t n_eq;
+    const int32_t eqr = base_eq + block_rank(eq, scratch, &n_eq);
+    const bool take = b < nb && (K >= nb || u > prefix || (eq && eqr < krem));
+    int32_t n_take;
+    const int32_t pos = base_sel + block_rank(take, scratch, &n_take);
+    if (take) keys[pos] = ((unsigned long long)u << 32) | (unsigned long long)(~(uint32_t)b);
+    base_eq += n_eq;
+    base_sel += n_take;
+  }
+  for (int32_t i = K + tid; i < kp2; i += blockDim.x) keys[i] = 0ull;
+  __syncthreads();
+  for (int32_t k = 2; k <= kp2; k <<= 1) {  // bitonic sort, descending
     for (int32_t j = k >> 1; j > 0; j >>= 1) {
-      for (int32_t i = threadIdx.x; i < np2; i += blockDim.x) {
+      for (int32_t i = tid; i < kp2; i += blockDim.x) {
         const int32_t ixj = i ^ j;
         if (ixj > i) {
           const unsigned long long x = keys[i], y = keys[ixj];
-          const bool desc = (i & k) == 0;
-          if (desc ? (x < y) : (x > y)) {
+          if (((i & k) == 0) ? (x < y) : (x > y)) {
             keys[i] = y;
             keys[ixj] = x;
           }
@@ -139,117 +259,86 @@ score_topk_kernel(Geom G, LayerState S, ReqTables RT, int32_t np2, const T* __re
       __syncthreads();
     }
   }
-
-  const int32_t n = nb < G.kb ? nb : G.kb;
-  for (int32_t i = threadIdx.x; i < n; i += blockDim.x) {
+  for (int32_t i = tid; i < K; i += blockDim.x) {
     const unsigned long long k = keys[i];
-    S.sel_ids[unit * G.kb + i] = (int32_t)(~(uint32_t)(k & 0xFFFFFFFFull));
+    const int32_t b = (int32_t)(~(uint32_t)(k & 0xFFFFFFFFull));
+    selid[i] = b;
+    S.sel_ids[unit * G.kb + i] = b;
     S.sel_scores[unit * G.kb + i] = from_orderable((uint32_t)(k >> 32));
   }
-  if (threadIdx.x == 0) S.n_sel[unit] = n;
-}
+  if (tid == 0) S.n_sel[unit] = K;
 
-// ---- diff / admit / evict ----------------------------------------------------------------
-//
-// One CTA per unit, one thread per slot (and per selection entry):
-//  hits (selected and resident) keep their slot and get stamp = step;
-//  misses are ranked in selection order and the first min(C, #misses) are admitted;
-//  targets are free slots by ascending slot, then unselected resident blocks by
-//  (stamp asc, block id asc); each admitted block takes the target of its rank, the evicted
-//  block leaves the resident map, and (block, slot) is appended to the fetch list.
-__global__ void select_kernel(Geom G, LayerState S, ReqTables RT, int32_t cap_blocks, int32_t step,
-                              Counters* ctr, int32_t* err) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  const int32_t kb = G.kb;
-  unsigned long long* tkey = reinterpret_cast<unsigned long long*>(smem);  // [kb]
-  int32_t* sb = reinterpret_cast<int32_t*>(tkey + kb);                     // [kb] slot -> block
-  int32_t* st = sb + kb;                                                   // [kb] stamps
-  int32_t* hit = st + kb;                                                  // [kb]
-  int32_t* target = hit + kb;                                              // [kb]
-  int32_t* warp_miss = target + kb;                                        // [32]
-
-  const int32_t a = blockIdx.x / G.Hkv, h = blockIdx.x % G.Hkv;
-  const int32_t r = RT.active[a];
-  const int64_t unit = (int64_t)r * G.Hkv + h;
-  const int32_t tid = threadIdx.x;
-  const int32_t n_sel = S.n_sel[unit];
-  const int32_t nb = (S.len[r] + G.bs - 1) / G.bs;
+  // ---- diff / admit / evict ----
   int16_t* resident = S.resident + unit * G.nb_max;
-
-  if (tid < kb) {
-    sb[tid] = S.slot_block[unit * kb + tid];
-    st[tid] = S.stamp[unit * kb + tid];
-    hit[tid] = 0;
+  for (int32_t s = tid; s < G.kb; s += blockDim.x) {
+    sb[s] = S.slot_block[unit * G.kb + s];
+    st[s] = S.stamp[unit * G.kb + s];
+    hit[s] = 0;
   }
   __syncthreads();
-
-  int32_t b = -1;
-  bool miss = false;
-  if (tid < n_sel) {
-    b = S.sel_ids[unit * kb + tid];
-    if (b < 0 || b >= nb || b >= G.nb_max) {
-      record_error(err, kErrBlockRange, -1, r, b);
-      b = -1;
+  for (int32_t i = tid; i < K; i += blockDim.x) {
+    const int32_t b = selid[i];
+    const int32_t s = resident[b];
+    missrank[i] = -1;
+    if (s >= G.kb) {
+      record_error(err, kErrSlotRange, -1, r, s);
+    } else if (s >= 0) {
+      hit[s] = 1;
+      st[s] = step;
     } else {
-      const int32_t s = resident[b];
-      if (s >= kb) {
-        record_error(err, kErrSlotRange, -1, r, s);
-      } else if (s >= 0) {
-        hit[s] = 1;
-        st[s] = step;
-      } else {
-        miss = true;
-      }
+      missrank[i] = 0;
     }
   }
-  // rank of each miss in selection order
-  const unsigned ballot = __ballot_sync(0xffffffffu, miss);
-  const int lane = tid & 31, warp = tid >> 5;
-  if (lane == 0) warp_miss[warp] = __popc(ballot);
   __syncthreads();
-  int32_t before = 0, n_miss = 0;
-  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
-    if (w < warp) before += warp_miss[w];
-    n_miss += warp_miss[w];
+  int32_t n_miss = 0;
+  for (int32_t i0 = 0; i0 < K; i0 += blockDim.x) {
+    const int32_t i = i0 + tid;
+    const bool miss = i < K && missrank[i] == 0;
+    int32_t n;
+    const int32_t rk = n_miss + block_rank(miss, scratch, &n);
+    if (miss) missrank[i] = rk;
+    n_miss += n;
   }
-  const int32_t rank = before + __popc(ballot & ((1u << lane) - 1u));
   const int32_t n_admit = n_miss < cap_blocks ? n_miss : cap_blocks;
-
-  // eviction-target keys: free slots (class 0, by slot), unselected resident (class 1)
-  if (tid < kb) {
+  for (int32_t s = tid; s < G.kb; s += blockDim.x) {
     unsigned long long k;
-    if (sb[tid] < 0)
-      k = (unsigned long long)tid;
-    else if (!hit[tid])
-      k = (1ull << 63) | ((unsigned long long)((uint32_t)st[tid] ^ 0x80000000u) << 31) |
-          (unsigned long long)(uint32_t)sb[tid];
+    if (sb[s] < 0)
+      k = (unsigned long long)s;  // free slots first, by slot
+    else if (!hit[s])
+      k = (1ull << 63) | ((unsigned long long)((uint32_t)st[s] ^ 0x80000000u) << 31) |
+          (unsigned long long)(uint32_t)sb[s];  // then least recently selected, by block id
     else
-      k = ~0ull;  // protected: never a target
-    tkey[tid] = k;
+      k = ~0ull;  // selected and resident: never a target
+    tkey[s] = k;
   }
   __syncthreads();
-  if (tid < kb && tkey[tid] != ~0ull) {
-    const unsigned long long mine = tkey[tid];
-    int32_t pos = 0;
-    for (int32_t o = 0; o < kb; ++o) pos += tkey[o] < mine;
-    if (pos < n_admit) target[pos] = tid;
+  if (n_admit > 0) {
+    for (int32_t s = tid; s < G.kb; s += blockDim.x) {
+      const unsigned long long mine = tkey[s];
+      if (mine == ~0ull) continue;
+      int32_t pos = 0;
+      for (int32_t o = 0; o < G.kb; ++o) pos += tkey[o] < mine;
+      if (pos < n_admit) target[pos] = s;
+    }
   }
   __syncthreads();
-
-  if (miss && rank < n_admit) {
-    const int32_t s = target[rank];
+  for (int32_t i = tid; i < K; i += blockDim.x) {
+    const int32_t rk = missrank[i];
+    if (rk < 0 || rk >= n_admit) continue;
+    const int32_t b = selid[i];
+    const int32_t s = target[rk];
     const int32_t old = sb[s];
     if (old >= 0) resident[old] = -1;
     resident[b] = (int16_t)s;
     sb[s] = b;
     st[s] = step;
-    S.fetch[(unit * kb + rank) * 2 + 0] = b;
-    S.fetch[(unit * kb + rank) * 2 + 1] = s;
+    S.fetch[(unit * G.kb + rk) * 2 + 0] = b;
+    S.fetch[(unit * G.kb + rk) * 2 + 1] = s;
   }
   __syncthreads();
-  if (tid < kb) {
-    S.slot_block[unit * kb + tid] = sb[tid];
-    S.stamp[unit * kb + tid] = st[tid];
+  for (int32_t s = tid; s < G.kb; s += blockDim.x) {
+    S.slot_block[unit * G.kb + s] = sb[s];
+    S.stamp[unit * G.kb + s] = st[s];
   }
   if (tid == 0) {
     S.n_fetch[unit] = n_admit;
@@ -259,38 +348,32 @@ __global__ void select_kernel(Geom G, LayerState S, ReqTables RT, int32_t cap_bl
 
 }  // namespace
 
-cudaError_t launch_score_topk(const Geom& G, const LayerState& S, const ReqTables& T,
-                              int32_t n_active, int32_t max_nb, const void* draft, int32_t* err,
-                              cudaStream_t s) {
+cudaError_t launch_stage(const Geom& G, const LayerState& S, const ReqTables& T, int32_t n_active,
+                         int32_t max_nb, const void* draft, uint32_t* scores, int32_t cap_blocks,
+                         int32_t step, Counters* ctr, int32_t* err, cudaStream_t s, int* n_launches) {
+  *n_launches = 0;
   if (n_active <= 0) return cudaSuccess;
-  int32_t np2 = 32;
-  while (np2 < max_nb) np2 <<= 1;
-  const size_t smem = (size_t)2 * G.d * sizeof(float) + (size_t)np2 * sizeof(unsigned long long);
-  const int grid = n_active * G.Hkv;
-  cudaError_t e;
-  if (G.dtype == OKV_F32) {
-    e = cudaFuncSetAttribute(score_topk_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
-    if (e != cudaSuccess) return e;
-    score_topk_kernel<float><<<grid, kScoreThreads, smem, s>>>(G, S, T, np2, (const float*)draft, err);
-  } else {
-    e = cudaFuncSetAttribute(score_topk_kernel<__nv_bfloat16>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    score_topk_kernel<__nv_bfloat16><<<grid, kScoreThreads, smem, s>>>(
-        G, S, T, np2, (const __nv_bfloat16*)draft, err);
-  }
-  return cudaGetLastError();
-}
-
-cudaError_t launch_select(const Geom& G, const LayerState& S, const ReqTables& T, int32_t n_active,
-                          int32_t cap_blocks, int32_t step, Counters* ctr, int32_t* err,
-                          cudaStream_t s) {
-  if (n_active <= 0) return cudaSuccess;
-  const int threads = ((G.kb + 31) / 32) * 32;
-  const size_t smem = (size_t)G.kb * (sizeof(unsigned long long) + 4 * sizeof(int32_t)) + 32 * sizeof(int32_t);
-  select_kernel<<<n_active * G.Hkv, threads, smem, s>>>(G, S, T, cap_blocks, step, ctr, err);
-  return cudaGetLastError();
+  const int32_t nb_cap = max_nb > 0 ? max_nb : 1;
+  const int32_t chunks = (nb_cap + kScoreChunk - 1) / kScoreChunk;
+  const size_t smem_score = (size_t)2 * G.d * 4;
+  const int units = n_active * G.Hkv;
+  if (G.dtype == OKV_F32)
+    score_kernel<float><<<units * chunks, kScoreThreads, smem_score, s>>>(G, S, T, chunks, (const float*)draft,
+                                                                       scores, err);
+  else
+    score_kernel<__nv_bfloat16><<<units * chunks, kScoreThreads, smem_score, s>>>(
+        G, S, T, chunks, (const __nv_bfloat16*)draft, scores, err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  int32_t kp2 = 1;
+  while (kp2 < G.kb) kp2 <<= 1;
+  const size_t smem = (size_t)(kp2 + G.kb) * 8 + (size_t)(nb_cap + 256) * 4 + (size_t)6 * G.kb * 4 + 36 * 4;
+  e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  select_kernel<<<units, kScoreThreads, smem, s>>>(G, S, T, nb_cap, kp2, scores, cap_blocks, step, ctr, err);
+  e = cudaGetLastError();
+  if (e == cudaSuccess) *n_launches = 2;
+  return e;
 }
 
 }  // namespace okv

@@ -14,6 +14,7 @@
 #include <math.h>
 #include <stdarg.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <chrono>
@@ -57,6 +58,8 @@ struct okv_ctx {
   void* partials = nullptr;
   size_t partials_bytes = 0;
   uint8_t* draft_buf = nullptr;  // [layers][R][Hq][d]: the staging's own copy of the draft queries
+  uint32_t* scores = nullptr;    // [R][Hkv][nb_max]: block score images of the layer being staged
+  bool stage_on_caller = false;  // run scoring/selection on the caller's stream (see okv_create)
   CUtensorMap pool_map;  // 64-byte aligned by its type
   bool have_map = false;
 
@@ -271,7 +274,7 @@ void okv_destroy(okv_ctx* c) {
   if (c->copy_stream) cudaStreamDestroy(c->copy_stream);
   void* bufs[] = {c->summ, c->pool, c->resident, c->slot_block, c->stamp, c->sel_ids, c->sel_scores,
                   c->n_sel, c->fetch, c->n_fetch, c->len, c->active_dev, c->host_kv_dev, c->cap_dev,
-                  c->err_dev, c->ctr_dev, c->partials, c->draft_buf};
+                  c->err_dev, c->ctr_dev, c->partials, c->draft_buf, c->scores};
   for (void* p : bufs)
     if (p) cudaFree(p);
   delete c;
@@ -339,7 +342,8 @@ okv_status okv_create(const okv_config* cfg, okv_ctx** out) {
             alloc((void**)&c->active_dev, G.R * 4) && alloc((void**)&c->host_kv_dev, G.R * 8) &&
             alloc((void**)&c->cap_dev, G.R * 4) && alloc((void**)&c->err_dev, 16) &&
             alloc((void**)&c->ctr_dev, sizeof(Counters)) &&
-            alloc((void**)&c->draft_buf, (size_t)L * G.R * G.Hq * G.d * G.elem);
+            alloc((void**)&c->draft_buf, (size_t)L * G.R * G.Hq * G.d * G.elem) &&
+            alloc((void**)&c->scores, (size_t)U * G.nb_max * sizeof(uint32_t));
   if (ok) {
     size_t ws = 0;
     for (int32_t n = 1; n <= G.R; ++n) {
@@ -369,8 +373,18 @@ okv_status okv_create(const okv_config* cfg, okv_ctx** out) {
   ck(cudaMemset(c->cap_dev, 0, G.R * 4));
   int lo = 0, hi = 0;
   ck(cudaDeviceGetStreamPriorityRange(&lo, &hi));
-  ck(cudaStreamCreateWithPriority(&c->sel_stream, cudaStreamNonBlocking, lo));
-  ck(cudaStreamCreateWithPriority(&c->copy_stream, cudaStreamNonBlocking, lo));
+  // staging streams run at the greatest priority: their kernels are short and the next step's
+  // attention of the layer waits on them (OKV_STAGE_PRIORITY=low puts them at the least)
+  const char* pe = getenv("OKV_STAGE_PRIORITY");
+  const int prio = (pe && strcmp(pe, "low") == 0) ? lo : hi;
+  // scoring and selection run on the caller's stream right after the layer's attention (both
+  // are bound by HBM bandwidth, so overlapping them buys nothing and they contend for SMs); only
+  // the host-link gather overlaps, on its own stream. OKV_STAGE_STREAM=internal moves scoring
+  // and selection to the internal select stream instead.
+  const char* ps = getenv("OKV_STAGE_STREAM");
+  c->stage_on_caller = !(ps && strcmp(ps, "internal") == 0);
+  ck(cudaStreamCreateWithPriority(&c->sel_stream, cudaStreamNonBlocking, prio));
+  ck(cudaStreamCreateWithPriority(&c->copy_stream, cudaStreamNonBlocking, prio));
   ck(cudaEventCreateWithFlags(&c->ev_in, cudaEventDisableTiming));
   c->ev_selected.assign(G.L, nullptr);
   c->ev_staged.assign(G.L, nullptr);
@@ -540,29 +554,35 @@ okv_status okv_stage(okv_ctx* c, int32_t layer, const void* draft_q, int32_t ste
   const int32_t n_active = (int32_t)c->active_list.size();
   if (n_active == 0) return OKV_OK;
   cudaStream_t s = (cudaStream_t)stream;
-  // the staging reads the draft later, on the select stream: take a copy on the caller's stream
-  // (after the previous staging of this layer has read its copy) so the caller may reuse its buffer
-  const size_t qbytes = (size_t)G.R * G.Hq * G.d * G.elem;
-  uint8_t* draft_copy = c->draft_buf + (size_t)layer * qbytes;
-  if (c->staged_once[layer]) OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_selected[layer], 0));
-  OKV_CUDA(c, cudaMemcpyAsync(draft_copy, draft_q, qbytes, cudaMemcpyDeviceToDevice, s));
-  OKV_CUDA(c, cudaEventRecord(c->ev_in, s));
-  OKV_CUDA(c, cudaStreamWaitEvent(c->sel_stream, c->ev_in, 0));
-  if (c->staged_once[layer]) OKV_CUDA(c, cudaStreamWaitEvent(c->sel_stream, c->ev_staged[layer], 0));
   const LayerState S = layer_state(c, layer);
   const ReqTables T = req_tables(c);
-  {
-    Timer t(c, OKV_K_SCORE_TOPK, c->sel_stream);
-    OKV_CUDA(c, okv::launch_score_topk(G, S, T, n_active, max_blocks_at(c, layer), draft_copy, c->err_dev,
-                                       c->sel_stream));
-    t.stop(1);
+  cudaStream_t ss = c->sel_stream;
+  const void* draft_src = draft_q;
+  if (c->stage_on_caller) {
+    // scoring and selection follow the caller's attention of this layer on its own stream
+    ss = s;
+    if (c->staged_once[layer]) OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_staged[layer], 0));
+  } else {
+    // the staging reads the draft later, on the select stream: take a copy on the caller's
+    // stream (after the previous staging of this layer has read its copy) so the caller may
+    // reuse its buffer
+    const size_t qbytes = (size_t)G.R * G.Hq * G.d * G.elem;
+    uint8_t* draft_copy = c->draft_buf + (size_t)layer * qbytes;
+    if (c->staged_once[layer]) OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_selected[layer], 0));
+    OKV_CUDA(c, cudaMemcpyAsync(draft_copy, draft_q, qbytes, cudaMemcpyDeviceToDevice, s));
+    OKV_CUDA(c, cudaEventRecord(c->ev_in, s));
+    OKV_CUDA(c, cudaStreamWaitEvent(ss, c->ev_in, 0));
+    if (c->staged_once[layer]) OKV_CUDA(c, cudaStreamWaitEvent(ss, c->ev_staged[layer], 0));
+    draft_src = draft_copy;
   }
   {
-    Timer t(c, OKV_K_SELECT, c->sel_stream);
-    OKV_CUDA(c, okv::launch_select(G, S, T, n_active, C, step, c->ctr_dev, c->err_dev, c->sel_stream));
-    t.stop(1);
+    Timer t(c, OKV_K_SCORE_TOPK, ss);
+    int n = 0;
+    OKV_CUDA(c, okv::launch_stage(G, S, T, n_active, max_blocks_at(c, layer), draft_src, c->scores, C, step,
+                                  c->ctr_dev, c->err_dev, ss, &n));
+    t.stop(n);
   }
-  OKV_CUDA(c, cudaEventRecord(c->ev_selected[layer], c->sel_stream));
+  OKV_CUDA(c, cudaEventRecord(c->ev_selected[layer], ss));
   OKV_CUDA(c, cudaStreamWaitEvent(c->copy_stream, c->ev_selected[layer], 0));
   {
     Timer t(c, OKV_K_GATHER, c->copy_stream);

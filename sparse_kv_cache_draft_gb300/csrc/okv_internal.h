@@ -72,12 +72,11 @@ cudaError_t launch_reset_request(const Geom& G, int16_t* resident, int32_t* slot
                                  int32_t req, int32_t n_tok, uint64_t host_kv, int32_t cap,
                                  uint64_t* host_kv_tab, int32_t* cap_tab, cudaStream_t s);
 cudaError_t launch_advance(const LayerState& S, const ReqTables& T, int32_t n_active, cudaStream_t s);
-cudaError_t launch_score_topk(const Geom& G, const LayerState& S, const ReqTables& T,
-                              int32_t n_active, int32_t max_nb, const void* draft,
-                              int32_t* err, cudaStream_t s);
-cudaError_t launch_select(const Geom& G, const LayerState& S, const ReqTables& T, int32_t n_active,
-                          int32_t cap_blocks, int32_t step, Counters* ctr, int32_t* err,
-                          cudaStream_t s);
+// Staging of one layer for every active unit: block scores (into `scores`, a [R][Hkv][nb_max]
+// uint32 workspace), then top-K and diff / admit / evict. Two launches.
+cudaError_t launch_stage(const Geom& G, const LayerState& S, const ReqTables& T, int32_t n_active,
+                         int32_t max_nb, const void* draft, uint32_t* scores, int32_t cap_blocks,
+                         int32_t step, Counters* ctr, int32_t* err, cudaStream_t s, int* n_launches);
 cudaError_t launch_gather(const Geom& G, const LayerState& S, const ReqTables& T, int32_t n_active,
                           int32_t layer, int32_t max_fetch, int32_t* err, cudaStream_t s);
 // Attention: decides between the tensor-core path (bf16, d = 128, g <= 8) and the CUDA-core

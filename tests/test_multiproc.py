@@ -1,0 +1,48 @@
+"""Replica plumbing of bench.py across processes (gloo, world size 2, CPU only).
+
+The staged path shards over requests with no data exchange, so several GPUs run independent
+replicas; the only cross-rank operations are a barrier and the max of the timed durations.
+"""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _worker(rank, world, port, q):
+    os.environ.update({"RANK": str(rank), "WORLD_SIZE": str(world), "LOCAL_RANK": str(rank),
+                       "MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
+    import bench
+    d = bench.Dist(want_gpu=False)
+    try:
+        d.barrier()
+        mx = d.max(1.5 + rank)
+        ref = bench.run_reference(type("A", (), {"alias": 1, "threads": 1, "warmup": 0, "steps": 1})(), d) \
+            if rank == 1 else "skipped"
+        q.put((rank, mx, ref))
+    finally:
+        d.close()
+
+
+def test_two_ranks_barrier_and_max():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=5) for _ in range(2))
+    assert [g[1] for g in got] == [2.5, 2.5]   # every rank sees the slowest rank's time
+    assert got[1][2] is None                   # the reference arm runs on rank 0 only
