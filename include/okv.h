@@ -186,6 +186,38 @@ OKV_API okv_status okv_read_timing(okv_ctx* ctx, okv_timing* out);
 /* Kernel launches made by this context so far (all kinds), counted on the host. */
 OKV_API int64_t okv_launch_count(const okv_ctx* ctx);
 
+/* ---- allocation-free attention (no counterpart in the paper) ----
+ *
+ * Some callers cannot call cudaMalloc: code that runs where allocation is forbidden or must
+ * not fail (a fixed memory budget handed over up front, an allocator they do not own, a
+ * graph or callback path that may not allocate). okv_attend_static gives them the sparse
+ * attention of okv_attend without a context and without allocating anything: the caller
+ * passes every input and output, and the kernels' only workspace (split partials, request ids,
+ * an error word) is one fixed 16 MiB device array inside this library, which every GPU that
+ * loads the library holds until the process exits.
+ *
+ *   pool:       device [n_requests][kv_heads][slots][2][block_size][head_dim] storage dtype,
+ *               16-byte aligned (the layout of one layer of okv's slot pool)
+ *   slot_block: device [n_requests][kv_heads][slots] int32, the block each slot holds or -1
+ *   lengths:    device [n_requests] int32, each request's context length in tokens
+ *   q, out:     device [n_requests][q_heads][head_dim] storage dtype
+ * Every request 0 .. n_requests-1 attends: softmax(q.k / sqrt(d)) v over every valid token of
+ * every occupied slot of its unit, zeros if none (the computation of okv_attend).
+ *
+ * Limits: n_requests <= 16384, and the split workspace the launch shape needs must fit in the
+ * array (about 16 MiB of n_requests * kv_heads * split * g * (head_dim + 2) floats); beyond
+ * them, and for shapes okv_create refuses, the call returns OKV_EINVAL without launching.
+ * The first call on a device resolves the array's device address (cudaGetSymbolAddress) and
+ * initialises its constant part, synchronising that device: make it before any stream
+ * capture. Later calls only enqueue on `stream`. All calls share the array: calls whose work
+ * overlaps on the GPU (on different streams, or on different host threads) race and must be
+ * serialised by the caller. Indices that fail the kernels' bounds checks are skipped; this
+ * call has no context to report them through. */
+OKV_API okv_status okv_attend_static(int32_t n_requests, int32_t q_heads, int32_t kv_heads,
+                                     int32_t head_dim, int32_t block_size, int32_t slots,
+                                     int32_t dtype, const void* pool, const int32_t* slot_block,
+                                     const int32_t* lengths, const void* q, void* out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -83,6 +83,7 @@ def load_library():
             "okv_set_timing": ([vp, i32], st),
             "okv_read_timing": ([vp, ctypes.POINTER(_Timing)], st),
             "okv_launch_count": ([vp], i64),
+            "okv_attend_static": ([i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp], st),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -315,3 +316,27 @@ class Context:
             self.close()
         except Exception:
             pass
+
+
+def attend_static(pool, slot_block, lengths, q, out, *, q_heads: int, kv_heads: int, head_dim: int,
+                  block_size: int, slots: int, dtype: int, stream=None) -> None:
+    """okv_attend_static: context-free sparse attention whose only workspace is the library's
+    fixed device array (nothing is allocated). Tensors are CUDA, contiguous:
+    pool [R][kv_heads][slots][2][block_size][head_dim] (bf16/fp32), slot_block [R][kv_heads][slots]
+    int32, lengths [R] int32, q and out [R][q_heads][head_dim]."""
+    import torch
+    L = load_library()
+    R = int(lengths.shape[0])
+    want = torch.float32 if dtype == F32 else torch.bfloat16
+    for name, t, shape, dt in (("pool", pool, (R, kv_heads, slots, 2, block_size, head_dim), want),
+                               ("slot_block", slot_block, (R, kv_heads, slots), torch.int32),
+                               ("lengths", lengths, (R,), torch.int32),
+                               ("q", q, (R, q_heads, head_dim), want), ("out", out, (R, q_heads, head_dim), want)):
+        if not t.is_cuda or t.dtype != dt or not t.is_contiguous() or tuple(t.shape) != shape:
+            raise ValueError(f"{name}: expected contiguous CUDA {dt} {shape}, got {t.dtype} {tuple(t.shape)}")
+    st = L.okv_attend_static(R, q_heads, kv_heads, head_dim, block_size, slots, dtype,
+                             ctypes.c_void_p(pool.data_ptr()), ctypes.c_void_p(slot_block.data_ptr()),
+                             ctypes.c_void_p(lengths.data_ptr()), ctypes.c_void_p(q.data_ptr()),
+                             ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(_stream_handle(stream)))
+    if st != OK:
+        raise OkvError(st, "okv_attend_static failed (shape or size outside its limits, or a CUDA error)")

@@ -21,6 +21,8 @@
 #include <stdio.h>
 #include <stdlib.h>
 
+#include <mutex>
+
 #include "okv_internal.h"
 
 namespace okv {
@@ -641,3 +643,135 @@ cudaError_t launch_attend(const Geom& G, const LayerState& S, const ReqTables& T
 }
 
 }  // namespace okv
+
+// ---- allocation-free variant ------------------------------------------------------------------
+//
+// For callers that cannot allocate device memory, okv_attend_static runs the same attention
+// kernels over caller-provided inputs and outputs. Its only workspace (the split partials,
+// the request-id list and the error word / counters the kernels write) lives in one fixed,
+// file-scope device array that every GPU loading this library holds until the process exits.
+
+namespace {
+
+constexpr size_t kStaticScratchBytes = (size_t)16 << 20;  // 16 MiB
+constexpr int32_t kStaticMaxRequests = 16384;
+constexpr size_t kStaticIdsOffset = 256;                  // [0, 256): error word, counters
+constexpr size_t kStaticPartialsOffset = kStaticIdsOffset + (size_t)kStaticMaxRequests * 4;
+
+static __device__ __align__(256) unsigned char okv_static_scratch[kStaticScratchBytes];
+
+__global__ void static_init_kernel(int32_t* ids, int32_t n, int32_t* err, okv::Counters* ctr) {
+  const int32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) ids[i] = i;
+  if (i < 4) err[i] = 0;
+  if (i == 0) {
+    ctr->fetched_blocks = 0;
+    ctr->attended_slots = 0;
+  }
+}
+
+std::mutex g_static_mu;
+void* g_static_base[256] = {};  // device address of okv_static_scratch, per device ordinal
+
+// Once per device, with that device current: resolve the array's device address (host code
+// cannot use the symbol itself) and fill the constant part (the request ids 0..max-1).
+cudaError_t static_scratch(void** base) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 256) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_base[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, okv_static_scratch);
+    if (e != cudaSuccess) return e;
+    unsigned char* b = static_cast<unsigned char*>(p);
+    static_init_kernel<<<(kStaticMaxRequests + 255) / 256, 256>>>(
+        reinterpret_cast<int32_t*>(b + kStaticIdsOffset), kStaticMaxRequests, reinterpret_cast<int32_t*>(b),
+        reinterpret_cast<okv::Counters*>(b + 16));
+    e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return e;
+    g_static_base[dev] = p;
+  }
+  *base = g_static_base[dev];
+  return cudaSuccess;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+}  // namespace
+
+extern "C" okv_status okv_attend_static(int32_t n_requests, int32_t q_heads, int32_t kv_heads,
+                                        int32_t head_dim, int32_t block_size, int32_t slots,
+                                        int32_t dtype, const void* pool, const int32_t* slot_block,
+                                        const int32_t* lengths, const void* q, void* out,
+                                        void* stream) {
+  using namespace okv;
+  if (n_requests <= 0 || n_requests > kStaticMaxRequests) return OKV_EINVAL;
+  if (q_heads <= 0 || kv_heads <= 0 || q_heads % kv_heads || q_heads / kv_heads > kMaxG) return OKV_EINVAL;
+  if (head_dim <= 0 || head_dim % 32 || head_dim > 256 || block_size <= 0 || block_size > 64) return OKV_EINVAL;
+  if (slots <= 0 || slots > 1024 || (dtype != OKV_F32 && dtype != OKV_BF16)) return OKV_EINVAL;
+  if (!pool || !slot_block || !lengths || !q || !out) return OKV_EINVAL;
+  Geom G{};
+  G.L = 1;
+  G.Hq = q_heads;
+  G.Hkv = kv_heads;
+  G.g = q_heads / kv_heads;
+  G.d = head_dim;
+  G.bs = block_size;
+  G.kb = slots;
+  G.R = n_requests;
+  G.nb_max = 0x3FFFFFFF;  // block ids are checked against each request's length only
+  G.dtype = dtype;
+  G.elem = dtype == OKV_F32 ? 4 : 2;
+  G.block_bytes = (int64_t)2 * block_size * head_dim * G.elem;
+  if ((block_size * head_dim * G.elem) % 16) return OKV_EINVAL;
+  // the split partials must fit in the fixed workspace
+  if (attend_workspace_bytes(G, n_requests) > kStaticScratchBytes - kStaticPartialsOffset) return OKV_EINVAL;
+
+  void* base = nullptr;
+  if (static_scratch(&base) != cudaSuccess) return OKV_ECUDA;
+  unsigned char* b = static_cast<unsigned char*>(base);
+  LayerState S{};
+  S.pool = static_cast<uint8_t*>(const_cast<void*>(pool));
+  S.slot_block = const_cast<int32_t*>(slot_block);
+  S.len = const_cast<int32_t*>(lengths);
+  ReqTables T{};
+  T.active = reinterpret_cast<const int32_t*>(b + kStaticIdsOffset);
+  CUtensorMap map;
+  const CUtensorMap* pmap = nullptr;
+  if (use_mma(G)) {
+    const uint64_t rows = (uint64_t)n_requests * kv_heads * slots * 32;
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || rows >= (1ull << 31) || (reinterpret_cast<uintptr_t>(pool) & 15)) return OKV_EINVAL;
+    const cuuint64_t dims[3] = {64, 2, rows};
+    const cuuint64_t strides[2] = {128, 256};
+    const cuuint32_t box[3] = {64, 2, 32};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (fn(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return OKV_EINVAL;
+    pmap = &map;
+  }
+  int n_launch = 0, split = 0;
+  cudaError_t e = launch_attend(G, S, T, n_requests, 0, q, out, pmap, b + kStaticPartialsOffset,
+                                reinterpret_cast<Counters*>(b + 16), reinterpret_cast<int32_t*>(b),
+                                (cudaStream_t)stream, &n_launch, &split);
+  return e == cudaSuccess ? OKV_OK : OKV_ECUDA;
+}
