@@ -57,6 +57,10 @@ def parse_args():
     p.add_argument("--batch", type=int, default=0, help="override the batch (smaller profiling cases)")
     p.add_argument("--layers", type=int, default=0, help="override the layer count (smaller profiling cases)")
     p.add_argument("--baseline-layers", type=int, default=6, help="layers in the cpu_baseline sample")
+    p.add_argument("--report", choices=["bench", "capsweep", "agreement"], default="bench",
+                   help="capsweep: bytes per step and tok/s per fetch cap (batch-90 sweep workload); "
+                        "agreement: draft vs previous-token top-K agreement with the true next query")
+    p.add_argument("--workload", default=None, help="synthetic workload name (default: the metric's)")
     return p.parse_args()
 
 
@@ -177,12 +181,13 @@ def pinned_h2d_gbs(nbytes=1 << 30, reps=5) -> float:
 # ---- workload setup ----------------------------------------------------------------------------
 
 class Workload:
-    def __init__(self, alias: int, threads: int, batch: int = 0, layers: int = 0):
+    def __init__(self, alias: int, threads: int, batch: int = 0, layers: int = 0, name: str | None = None):
         import numpy as np
         import synth
         self.np = np
         self.synth = synth
-        self.w = synth.WORKLOADS[WORKLOAD]
+        self.name = name or WORKLOAD
+        self.w = synth.WORKLOADS[self.name]
         if batch:
             self.w = self.w.scaled(batch=batch)
         if layers:
@@ -220,7 +225,9 @@ class Workload:
 
     def config_json(self):
         w = self.w
-        return {"workload": WORKLOAD if (self.B, self.L) == (128, 36) else f"{WORKLOAD} (batch {self.B}, {self.L} layers)",
+        ref = self.synth.WORKLOADS[self.name]
+        full = (self.B, self.L) == (ref.batch, ref.layers)
+        return {"workload": self.name if full else f"{self.name} (batch {self.B}, {self.L} layers)",
                 "model_shapes": "Qwen3-8B attention", "batch": self.B, "seq_len": self.n_tok,
                 "layers": self.L, "q_heads": self.Hq, "kv_heads": self.Hkv, "head_dim": self.d,
                 "block_size": w.block_size, "budget_tokens": w.budget_tokens, "fetch_cap": w.fetch_cap,
@@ -284,7 +291,7 @@ def run_okv(args, dist: Dist):
 
     load_library()
     torch.cuda.set_device(dist.local)
-    wl = Workload(args.alias, args.threads, args.batch, args.layers)
+    wl = Workload(args.alias, args.threads, args.batch, args.layers, args.workload)
     cfg = wl.config()
     B, L, Hq, d = wl.B, wl.L, wl.Hq, wl.d
     K, W = args.steps, args.warmup
@@ -430,7 +437,7 @@ def run_okv(args, dist: Dist):
 def run_reference(args, dist: Dist):
     if dist.rank != 0:
         return None
-    wl = Workload(args.alias, args.threads, args.batch, args.layers)
+    wl = Workload(args.alias, args.threads, args.batch, args.layers, args.workload)
     bufs = wl.host_kv()
     n_layers_used = min(4, wl.L)
     t = OracleTimer(wl, bufs, range(n_layers_used))
@@ -454,11 +461,132 @@ def run_reference(args, dist: Dist):
             "e2e": {"value": round(value, 3), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def _setup_context(wl, bufs, cap=None):
+    from sparse_kv_cache_draft_gb300 import Context
+    cfg = wl.config()
+    if cap is not None:
+        cfg.fetch_cap = cap
+    ctx = Context(cfg)
+    for r in range(wl.B):
+        ctx.add_request(r, bufs[int(wl.keys[r])].ptr, wl.nb, wl.n_tok)
+    return ctx
+
+
+def _device_inputs(wl, steps):
+    """bf16 device tensors q[t] (steps 0..steps-1) and dr[t + 1] = draft of step t (t = -1..steps-1)."""
+    import numpy as np
+    import torch
+    shape = (wl.L, wl.B, wl.Hq, wl.d)
+    qh = np.empty((steps,) + shape, np.uint16)
+    dh = np.empty((steps + 1,) + shape, np.uint16)
+    for t in range(-1, steps):
+        for l in range(wl.L):
+            if t >= 0:
+                wl.queries(l, t, 0, out=qh[t, l])
+            wl.queries(l, t, 1, out=dh[t + 1, l])
+    conv = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to("cuda")
+    return conv(qh), conv(dh)
+
+
+def run_capsweep(args, dist: Dist):
+    """Fetch-cap sweep: bytes moved host->HBM per step and decode tok/s per cap."""
+    import torch
+    name = args.workload or "qwen3_8b_capsweep_b90"
+    wl = Workload(args.alias, args.threads, args.batch, args.layers, name)
+    bufs = wl.host_kv()
+    K, W = args.steps, args.warmup
+    q, dr = _device_inputs(wl, W + K)
+    out = torch.empty(q.shape[1:], dtype=torch.bfloat16, device="cuda")
+    rows = []
+    for cap in wl.w.caps:
+        ctx = _setup_context(wl, bufs, cap)
+        for l in range(wl.L):
+            ctx.stage(l, dr[0, l], 0, 1.0)
+        for t in range(W):
+            ctx.step(q[t], dr[t + 1], out, t + 1)
+        torch.cuda.synchronize()
+        ctx.set_timing(True)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for t in range(W, W + K):
+            ctx.step(q[t], dr[t + 1], out, t + 1)
+        ctx.join()
+        e1.record()
+        e1.synchronize()
+        ms = dist.max(e0.elapsed_time(e1))
+        tm = ctx.read_timing()
+        gb = tm["fetched_blocks"] * 2 * wl.w.block_size * wl.d * 2 / K / 1e9
+        rows.append({"fetch_cap": cap, "C_blocks": max(1, int(cap * wl.kb)), "gb_per_step": round(gb, 4),
+                     "tok_s": round(dist.world * wl.B * K / (ms / 1e3), 1), "ms_per_step": round(ms / K, 4),
+                     "gather_gbs": round(gb * K / (tm["ms"]["gather"] / 1e3), 1) if tm["ms"]["gather"] else None})
+        ctx.close()
+    for b in bufs:
+        b.free()
+    return {"report": "capsweep", "metric": "sparse-decode tok/s and host->HBM GB/step per fetch cap",
+            "unit": "tok/s", "n_gpus": dist.world, "steps": K, "warmup": W, "data": "synthetic",
+            "config": wl.config_json(), "caps": rows}
+
+
+def run_agreement(args, dist: Dist):
+    """Per layer: overlap of the top-K the staging selects from the draft of step t with the top-K of
+    the true query of step t+1, against the previous-token proxy (the query of step t)."""
+    import numpy as np
+    import torch
+    wl = Workload(args.alias, args.threads, args.batch, args.layers, args.workload)
+    bufs = wl.host_kv()
+    K = args.steps
+    q, dr = _device_inputs(wl, K + 1)
+    ctx = _setup_context(wl, bufs)
+    out = torch.empty(q.shape[1:], dtype=torch.bfloat16, device="cuda")
+    counts = torch.zeros((wl.B, wl.Hkv), dtype=torch.int32, device="cuda")
+    ids = torch.zeros((wl.B, wl.Hkv, wl.kb), dtype=torch.int32, device="cuda")
+
+    def overlap(a_cnt, a_ids, b_cnt, b_ids):
+        tot = hit = 0
+        for r in range(wl.B):
+            for h in range(wl.Hkv):
+                n = int(a_cnt[r, h])
+                hit += len(set(a_ids[r, h, :n].tolist()) & set(b_ids[r, h, :int(b_cnt[r, h])].tolist()))
+                tot += n
+        return hit / max(tot, 1)
+
+    for l in range(wl.L):
+        ctx.stage(l, dr[0, l], 0, 1.0)
+    draft_agree = np.zeros((K, wl.L))
+    proxy_agree = np.zeros((K, wl.L))
+    for t in range(K):
+        for l in range(wl.L):
+            ctx.attend(l, q[t, l], out[l])
+            ctx.stage(l, dr[t + 1, l], t + 1)
+            torch.cuda.synchronize()
+            d_cnt, d_ids, _ = ctx.read_selection(l)
+            ctx.predict(l, q[t + 1, l], counts, ids)
+            true_cnt, true_ids = counts.cpu().numpy().copy(), ids.cpu().numpy().copy()
+            ctx.predict(l, q[t, l], counts, ids)
+            prev_cnt, prev_ids = counts.cpu().numpy(), ids.cpu().numpy()
+            draft_agree[t, l] = overlap(d_cnt, d_ids, true_cnt, true_ids)
+            proxy_agree[t, l] = overlap(prev_cnt, prev_ids, true_cnt, true_ids)
+    ctx.close()
+    for b in bufs:
+        b.free()
+    return {"report": "agreement", "metric": "top-K agreement with the true next query", "unit": "fraction",
+            "steps": K, "data": "synthetic", "config": wl.config_json(),
+            "draft_mean": round(float(draft_agree.mean()), 4), "draft_min_layer": round(float(draft_agree.mean(0).min()), 4),
+            "proxy_mean": round(float(proxy_agree.mean()), 4), "proxy_min_layer": round(float(proxy_agree.mean(0).min()), 4),
+            "draft_per_layer": [round(float(x), 4) for x in draft_agree.mean(0)],
+            "proxy_per_layer": [round(float(x), 4) for x in proxy_agree.mean(0)]}
+
+
 def main():
     args = parse_args()
     dist = Dist(want_gpu=args.impl == "okv")
     try:
-        res = run_okv(args, dist) if args.impl == "okv" else run_reference(args, dist)
+        if args.report == "capsweep":
+            res = run_capsweep(args, dist) if dist.rank == 0 else None
+        elif args.report == "agreement":
+            res = run_agreement(args, dist) if dist.rank == 0 else None
+        else:
+            res = run_okv(args, dist) if args.impl == "okv" else run_reference(args, dist)
         if res is not None and dist.rank == 0:
             print(json.dumps(res), flush=True)
     finally:

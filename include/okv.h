@@ -126,6 +126,24 @@ OKV_API okv_status okv_stage(okv_ctx* ctx, int32_t layer, const void* draft_q, i
  * staging. Rows of inactive requests are not written. */
 OKV_API okv_status okv_attend(okv_ctx* ctx, int32_t layer, const void* q, void* out, void* stream);
 
+/* Top-K prediction alone ("4 System Design": top-K prediction, the first link of the per-layer
+ * chain) for any query, e.g. the true next query or the previous token's query, to measure how
+ * well a draft predicts the blocks a step attends. query: device [max_requests][q_heads]
+ * [head_dim]; counts: device [max_requests][kv_heads] int32; ids: device [max_requests]
+ * [kv_heads][Kb] int32, the selected block ids in (score desc, id asc) order. The context's
+ * selections, slot tables and pools are not changed. Ordered after the work on `stream`;
+ * `stream` waits for the result. */
+OKV_API okv_status okv_predict(okv_ctx* ctx, int32_t layer, const void* query, int32_t* counts, int32_t* ids,
+                               void* stream);
+
+/* Look-ahead attention ("4 System Design": normal and draft queries are computed together over
+ * the resident KV): okv_attend for q -> out and, over the same resident set, for draft_q ->
+ * draft_out (both device [max_requests][q_heads][head_dim]). When twice the GQA group fits the
+ * tensor-core tile (2g <= 8) both are computed in one pass over K and V; otherwise the draft
+ * heads take a second pass. */
+OKV_API okv_status okv_attend_lookahead(okv_ctx* ctx, int32_t layer, const void* q, const void* draft_q,
+                                        void* out, void* draft_out, void* stream);
+
 /* One decode step over every layer, in layer order ("4 System Design": the foreground waits
  * only for each layer's transfer; the background chain of layer l overlaps the attention of the
  * later layers): for l = 0 .. layers-1: okv_append(l) if k_new is not NULL, okv_attend(l),

@@ -71,6 +71,8 @@ def load_library():
             "okv_append": ([vp, i32, vp, vp, vp], st),
             "okv_stage": ([vp, i32, vp, i32, f32, vp], st),
             "okv_attend": ([vp, i32, vp, vp, vp], st),
+            "okv_attend_lookahead": ([vp, i32, vp, vp, vp, vp, vp], st),
+            "okv_predict": ([vp, i32, vp, vp, vp, vp], st),
             "okv_step": ([vp, vp, vp, vp, vp, vp, i32, f32, vp], st),
             "okv_sync": ([vp, i64], st),
             "okv_join": ([vp, vp], st),
@@ -230,6 +232,25 @@ class Context:
         self._check(self.L.okv_attend(self.h, layer, self._tensor_ptr(q, self._qshape, "q"),
                                       self._tensor_ptr(out, self._qshape, "out"),
                                       ctypes.c_void_p(_stream_handle(stream))), "okv_attend")
+
+    def predict(self, layer: int, query, counts, ids, stream=None):
+        """Top-K of `query` into device int32 tensors counts [R][Hkv] and ids [R][Hkv][Kb]."""
+        import torch
+        c = self.cfg
+        for name, t, shp in (("counts", counts, (c.max_requests, c.kv_heads)),
+                             ("ids", ids, (c.max_requests, c.kv_heads, c.slots))):
+            if not t.is_cuda or t.dtype != torch.int32 or not t.is_contiguous() or tuple(t.shape) != shp:
+                raise ValueError(f"{name}: expected contiguous CUDA int32 {shp}")
+        self._check(self.L.okv_predict(self.h, layer, self._tensor_ptr(query, self._qshape, "query"),
+                                       ctypes.c_void_p(counts.data_ptr()), ctypes.c_void_p(ids.data_ptr()),
+                                       ctypes.c_void_p(_stream_handle(stream))), "okv_predict")
+
+    def attend_lookahead(self, layer: int, q, draft, out, draft_out, stream=None):
+        self._check(self.L.okv_attend_lookahead(self.h, layer, self._tensor_ptr(q, self._qshape, "q"),
+                                                self._tensor_ptr(draft, self._qshape, "draft"),
+                                                self._tensor_ptr(out, self._qshape, "out"),
+                                                self._tensor_ptr(draft_out, self._qshape, "draft_out"),
+                                                ctypes.c_void_p(_stream_handle(stream))), "okv_attend_lookahead")
 
     def step(self, q, draft, out, step: int, fetch_cap: float = -1.0, k_new=None, v_new=None, stream=None):
         c = self.cfg

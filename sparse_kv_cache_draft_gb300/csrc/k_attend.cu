@@ -159,6 +159,63 @@ __device__ int32_t build_items(const Geom& G, const int32_t* slot_block, int32_t
   return base;
 }
 
+// The rows one unit's attention computes: rows 0..g-1 are the group's query heads of q; with a
+// draft query (look-ahead attention) rows g..2g-1 are the same heads of the draft, attending
+// over the same resident K and V.
+template <typename T>
+struct Rows {
+  const T* q;
+  const T* dq;  // NULL: no draft rows
+  T* out;
+  T* dout;
+  int32_t n;    // g or 2g
+  __device__ __forceinline__ const T* in(const Geom& G, int32_t r, int32_t h, int32_t j) const {
+    return (j < G.g ? q : dq) + ((int64_t)r * G.Hq + h * G.g + (j < G.g ? j : j - G.g)) * G.d;
+  }
+  __device__ __forceinline__ T* dst(const Geom& G, int32_t r, int32_t h, int32_t j) const {
+    return (j < G.g ? out : dout) + ((int64_t)r * G.Hq + h * G.g + (j < G.g ? j : j - G.g)) * G.d;
+  }
+};
+
+__device__ __forceinline__ void store_out(float* p, float x) { *p = x; }
+__device__ __forceinline__ void store_out(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+
+// The split partials of unit `ua` are complete when the last of its `split` CTAs arrives; that
+// CTA merges the (max, sum, o) triples and writes the output. Returns false in the other CTAs.
+template <typename T>
+__device__ bool finish_split(const Geom& G, int32_t r, int32_t h, int32_t ua, int32_t split,
+                             const float* __restrict__ partials, int32_t* __restrict__ arrivals,
+                             const Rows<T>& rows) {
+  __shared__ int32_t last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    last = atomicAdd(&arrivals[ua], 1) == split - 1;
+    if (last) arrivals[ua] = 0;
+  }
+  __syncthreads();
+  if (!last) return false;
+  __threadfence();
+  const int32_t nr = rows.n;
+  const int64_t stride = (int64_t)nr * (G.d + 2);
+  const float* base = partials + (int64_t)ua * split * stride;
+  for (int32_t idx = threadIdx.x; idx < nr * G.d; idx += blockDim.x) {
+    const int head = idx / G.d, dim = idx % G.d;
+    float M = -INFINITY;
+    for (int p = 0; p < split; ++p) M = fmaxf(M, __ldcg(base + p * stride + nr * G.d + head));
+    float acc = 0.f, l = 0.f;
+    if (M != -INFINITY) {
+      for (int p = 0; p < split; ++p) {
+        const float f = exp2f(__ldcg(base + p * stride + nr * G.d + head) - M);
+        acc += f * __ldcg(base + p * stride + head * G.d + dim);
+        l += f * __ldcg(base + p * stride + nr * G.d + nr + head);
+      }
+    }
+    store_out(rows.dst(G, r, h, head) + dim, l > 0.f ? acc / l : 0.f);
+  }
+  return true;
+}
+
 // ---- tensor-core path ------------------------------------------------------------------------
 
 template <int NW, int NS>
@@ -171,8 +228,8 @@ struct MmaSmem {
 template <int NW, int NS>
 __global__ void __launch_bounds__(NW * 32)
 attend_mma_kernel(Geom G, LayerState S, ReqTables RT, const __grid_constant__ CUtensorMap pool_map,
-                  int64_t row_base, int32_t split, const __nv_bfloat16* __restrict__ q,
-                  __nv_bfloat16* __restrict__ out, float* __restrict__ partials, Counters* ctr,
+                  int64_t row_base, int32_t split, const Rows<__nv_bfloat16> rows,
+                  float* __restrict__ partials, int32_t* __restrict__ arrivals, Counters* ctr,
                   int32_t* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -215,8 +272,8 @@ attend_mma_kernel(Geom G, LayerState S, ReqTables RT, const __grid_constant__ CU
   // query fragments (B operand of QK^T): head gi of the group, dims in the permuted k order
   uint32_t qb[8][2];
   {
-    const bool real = gi < G.g;
-    const __nv_bfloat16* qh = q + ((int64_t)r * G.Hq + h * G.g + (real ? gi : 0)) * kMmaD;
+    const bool real = gi < rows.n;
+    const __nv_bfloat16* qh = rows.in(G, r, h, real ? gi : 0);
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
@@ -356,7 +413,8 @@ attend_mma_kernel(Geom G, LayerState S, ReqTables RT, const __grid_constant__ CU
     }
   }
   __syncthreads();
-  const int32_t nval = G.g * kMmaD;
+  const int32_t nr = rows.n;
+  const int32_t nval = nr * kMmaD;
   for (int32_t idx = threadIdx.x; idx < nval; idx += blockDim.x) {
     const int head = idx / kMmaD, dim = idx % kMmaD;
     float M = -INFINITY;
@@ -372,17 +430,18 @@ attend_mma_kernel(Geom G, LayerState S, ReqTables RT, const __grid_constant__ CU
       }
     }
     if (split == 1) {
-      out[((int64_t)r * G.Hq + h * G.g + head) * kMmaD + dim] = __float2bfloat16_rn(l > 0.f ? acc / l : 0.f);
+      rows.dst(G, r, h, head)[dim] = __float2bfloat16_rn(l > 0.f ? acc / l : 0.f);
     } else {
       const int64_t pu = (int64_t)ua * split + part;
-      float* po = partials + pu * G.g * (kMmaD + 2);
+      float* po = partials + pu * nr * (kMmaD + 2);
       po[head * kMmaD + dim] = acc;
       if (dim == 0) {
-        po[G.g * kMmaD + head] = M;
-        po[G.g * kMmaD + G.g + head] = l;
+        po[nr * kMmaD + head] = M;
+        po[nr * kMmaD + nr + head] = l;
       }
     }
   }
+  if (split > 1) finish_split(G, r, h, ua, split, partials, arrivals, rows);
 }
 
 // ---- CUDA-core path ---------------------------------------------------------------------------
@@ -397,14 +456,16 @@ constexpr int kSimtMaxDv = 8;  // head_dim <= 256
 
 template <typename T>
 __global__ void __launch_bounds__(kSimtWarps * 32)
-attend_simt_kernel(Geom G, LayerState S, ReqTables RT, int32_t split, const T* __restrict__ q,
-                   T* __restrict__ out, float* __restrict__ partials, Counters* ctr, int32_t* err) {
+attend_simt_kernel(Geom G, LayerState S, ReqTables RT, int32_t split, const Rows<T> rows,
+                   float* __restrict__ partials, int32_t* __restrict__ arrivals, Counters* ctr,
+                   int32_t* err) {
   extern __shared__ __align__(16) uint8_t smem[];
   int32_t* items = reinterpret_cast<int32_t*>(smem);   // [kb]
   int32_t* scratch = items + G.kb;                     // [32]
-  float* ow = reinterpret_cast<float*>(scratch + 32);  // [NW][g][d]
-  float* mw = ow + kSimtWarps * G.g * G.d;             // [NW][g]
-  float* lw = mw + kSimtWarps * G.g;                   // [NW][g]
+  float* ow = reinterpret_cast<float*>(scratch + 32);  // [NW][rows][d]
+  const int32_t nr = rows.n;
+  float* mw = ow + kSimtWarps * nr * G.d;              // [NW][rows]
+  float* lw = mw + kSimtWarps * nr;                    // [NW][rows]
 
   const int32_t ua = blockIdx.x / split, part = blockIdx.x % split;
   const int32_t a = ua / G.Hkv, h = ua % G.Hkv;
@@ -428,7 +489,7 @@ attend_simt_kernel(Geom G, LayerState S, ReqTables RT, int32_t split, const T* _
 #pragma unroll
     for (int i = 0; i < kSimtMaxDv; ++i) {
       ov[j][i] = 0.f;
-      qv[j][i] = (j < G.g && i < dv) ? ld_f(q + ((int64_t)r * G.Hq + h * G.g + j) * G.d + lane + 32 * i) * scale : 0.f;
+      qv[j][i] = (j < nr && i < dv) ? ld_f(rows.in(G, r, h, j) + lane + 32 * i) * scale : 0.f;
     }
   }
   for (int32_t it = warp; it < n_items; it += kSimtWarps) {
@@ -444,7 +505,7 @@ attend_simt_kernel(Geom G, LayerState S, ReqTables RT, int32_t split, const T* _
       }
 #pragma unroll
       for (int j = 0; j < kMaxG; ++j) {
-        if (j >= G.g) break;
+        if (j >= nr) break;
         float s = 0.f;
 #pragma unroll
         for (int i = 0; i < kSimtMaxDv; ++i) s = fmaf(qv[j][i], kx[i], s);
@@ -461,66 +522,41 @@ attend_simt_kernel(Geom G, LayerState S, ReqTables RT, int32_t split, const T* _
   }
 #pragma unroll
   for (int j = 0; j < kMaxG; ++j) {
-    if (j >= G.g) break;
+    if (j >= nr) break;
 #pragma unroll
     for (int i = 0; i < kSimtMaxDv; ++i)
-      if (i < dv) ow[(warp * G.g + j) * G.d + lane + 32 * i] = ov[j][i];
+      if (i < dv) ow[(warp * nr + j) * G.d + lane + 32 * i] = ov[j][i];
     if (lane == 0) {
-      mw[warp * G.g + j] = m[j];
-      lw[warp * G.g + j] = l[j];
+      mw[warp * nr + j] = m[j];
+      lw[warp * nr + j] = l[j];
     }
   }
   __syncthreads();
-  for (int32_t idx = threadIdx.x; idx < G.g * G.d; idx += blockDim.x) {
+  for (int32_t idx = threadIdx.x; idx < nr * G.d; idx += blockDim.x) {
     const int head = idx / G.d, dim = idx % G.d;
     float M = -INFINITY;
-    for (int w = 0; w < kSimtWarps; ++w) M = fmaxf(M, mw[w * G.g + head]);
+    for (int w = 0; w < kSimtWarps; ++w) M = fmaxf(M, mw[w * nr + head]);
     float acc = 0.f, ls = 0.f;
     if (M != -INFINITY) {
       for (int w = 0; w < kSimtWarps; ++w) {
-        const float f = exp2f(mw[w * G.g + head] - M);
-        acc += f * ow[(w * G.g + head) * G.d + dim];
-        ls += f * lw[w * G.g + head];
+        const float f = exp2f(mw[w * nr + head] - M);
+        acc += f * ow[(w * nr + head) * G.d + dim];
+        ls += f * lw[w * nr + head];
       }
     }
     if (split == 1) {
-      st_f(out + ((int64_t)r * G.Hq + h * G.g + head) * G.d + dim, ls > 0.f ? acc / ls : 0.f);
+      st_f(rows.dst(G, r, h, head) + dim, ls > 0.f ? acc / ls : 0.f);
     } else {
       const int64_t pu = (int64_t)ua * split + part;
-      float* po = partials + pu * G.g * (G.d + 2);
+      float* po = partials + pu * nr * (G.d + 2);
       po[head * G.d + dim] = acc;
       if (dim == 0) {
-        po[G.g * G.d + head] = M;
-        po[G.g * G.d + G.g + head] = ls;
+        po[nr * G.d + head] = M;
+        po[nr * G.d + nr + head] = ls;
       }
     }
   }
-}
-
-// ---- split combine ------------------------------------------------------------------------------
-
-template <typename T>
-__global__ void combine_kernel(Geom G, ReqTables RT, int32_t split, const float* __restrict__ partials,
-                               T* __restrict__ out) {
-  const int32_t ua = blockIdx.x;
-  const int32_t a = ua / G.Hkv, h = ua % G.Hkv;
-  const int32_t r = RT.active[a];
-  const int64_t stride = (int64_t)G.g * (G.d + 2);
-  const float* base = partials + (int64_t)ua * split * stride;
-  for (int32_t idx = threadIdx.x; idx < G.g * G.d; idx += blockDim.x) {
-    const int head = idx / G.d, dim = idx % G.d;
-    float M = -INFINITY;
-    for (int p = 0; p < split; ++p) M = fmaxf(M, base[p * stride + G.g * G.d + head]);
-    float acc = 0.f, l = 0.f;
-    if (M != -INFINITY) {
-      for (int p = 0; p < split; ++p) {
-        const float f = exp2f(base[p * stride + G.g * G.d + head] - M);
-        acc += f * base[p * stride + head * G.d + dim];
-        l += f * base[p * stride + G.g * G.d + G.g + head];
-      }
-    }
-    st_f(out + ((int64_t)r * G.Hq + h * G.g + head) * G.d + dim, l > 0.f ? acc / l : 0.f);
-  }
+  if (split > 1) finish_split(G, r, h, ua, split, partials, arrivals, rows);
 }
 
 // Tile shape of the tensor-core path, chosen at first use (OKV_ATTEND_TILE=<warps>x<stages>).
@@ -563,8 +599,8 @@ int32_t pick_split(const Geom& G, int32_t n_active, int ctas_per_sm, int warps) 
 
 template <int NW, int NS>
 cudaError_t run_mma(const Geom& G, const LayerState& S, const ReqTables& T, int32_t n_active,
-                    int32_t layer, const void* q, void* out, const CUtensorMap* map, void* partials,
-                    Counters* ctr, int32_t* err, cudaStream_t s, int32_t split) {
+                    int32_t layer, const Rows<__nv_bfloat16>& rows, const CUtensorMap* map, void* partials,
+                    int32_t* arrivals, Counters* ctr, int32_t* err, cudaStream_t s, int32_t split) {
   const size_t smem = MmaSmem<NW, NS>::bytes(G.kb);
   cudaError_t e = cudaFuncSetAttribute(attend_mma_kernel<NW, NS>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -572,9 +608,54 @@ cudaError_t run_mma(const Geom& G, const LayerState& S, const ReqTables& T, int3
   // the pool tensor map spans every layer: rows of 256 bytes, 32 rows (K then V) per slot
   const int64_t row_base = (int64_t)layer * G.R * G.Hkv * G.kb * 32;
   attend_mma_kernel<NW, NS><<<n_active * G.Hkv * split, NW * 32, smem, s>>>(
-      G, S, T, *map, row_base, split, (const __nv_bfloat16*)q, (__nv_bfloat16*)out,
-      (float*)partials, ctr, err);
+      G, S, T, *map, row_base, split, rows, (float*)partials, arrivals, ctr, err);
   return cudaGetLastError();
+}
+
+// One attention launch over `nrows` rows (the group's heads of q, then, if dq is given, of dq).
+cudaError_t launch_rows(const Geom& G, const LayerState& S, const ReqTables& T, int32_t n_active,
+                        int32_t layer, const void* q, const void* dq, void* out, void* dout, int32_t nrows,
+                        const CUtensorMap* pool_map, void* partials, int32_t* arrivals, Counters* ctr,
+                        int32_t* err, cudaStream_t s, int32_t* used_split) {
+  cudaError_t e;
+  int32_t split;
+  if (use_mma(G)) {
+    const Rows<__nv_bfloat16> rows{(const __nv_bfloat16*)q, (const __nv_bfloat16*)dq, (__nv_bfloat16*)out,
+                                   (__nv_bfloat16*)dout, nrows};
+    const MmaShape sh = mma_shape();
+    split = pick_split(G, n_active, 2, sh.nw);
+    if (sh.nw == 8 && sh.ns == 2)
+      e = run_mma<8, 2>(G, S, T, n_active, layer, rows, pool_map, partials, arrivals, ctr, err, s, split);
+    else if (sh.nw == 8 && sh.ns == 3)
+      e = run_mma<8, 3>(G, S, T, n_active, layer, rows, pool_map, partials, arrivals, ctr, err, s, split);
+    else if (sh.ns == 2)
+      e = run_mma<4, 2>(G, S, T, n_active, layer, rows, pool_map, partials, arrivals, ctr, err, s, split);
+    else if (sh.ns == 4)
+      e = run_mma<4, 4>(G, S, T, n_active, layer, rows, pool_map, partials, arrivals, ctr, err, s, split);
+    else
+      e = run_mma<4, 3>(G, S, T, n_active, layer, rows, pool_map, partials, arrivals, ctr, err, s, split);
+  } else {
+    split = pick_split(G, n_active, 4, kSimtWarps);
+    const size_t smem = (size_t)(G.kb + 32) * 4 + (size_t)kSimtWarps * nrows * (G.d + 2) * 4;
+    const int grid = n_active * G.Hkv * split;
+    if (G.dtype == OKV_F32) {
+      const Rows<float> rows{(const float*)q, (const float*)dq, (float*)out, (float*)dout, nrows};
+      e = cudaFuncSetAttribute(attend_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e == cudaSuccess)
+        attend_simt_kernel<float><<<grid, kSimtWarps * 32, smem, s>>>(G, S, T, split, rows, (float*)partials,
+                                                                      arrivals, ctr, err);
+    } else {
+      const Rows<__nv_bfloat16> rows{(const __nv_bfloat16*)q, (const __nv_bfloat16*)dq, (__nv_bfloat16*)out,
+                                     (__nv_bfloat16*)dout, nrows};
+      e = cudaFuncSetAttribute(attend_simt_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e == cudaSuccess)
+        attend_simt_kernel<__nv_bfloat16><<<grid, kSimtWarps * 32, smem, s>>>(G, S, T, split, rows,
+                                                                              (float*)partials, arrivals, ctr, err);
+    }
+    if (e == cudaSuccess) e = cudaGetLastError();
+  }
+  *used_split = split;
+  return e;
 }
 
 }  // namespace
@@ -585,61 +666,35 @@ size_t attend_workspace_bytes(const Geom& G, int32_t n_active) {
   const int warps = use_mma(G) ? mma_shape().nw : kSimtWarps;
   const int32_t n = n_active > 0 ? n_active : 1;
   const int32_t split = pick_split(G, n, use_mma(G) ? 2 : 4, warps);
-  return (size_t)n * G.Hkv * split * G.g * (G.d + 2) * sizeof(float);
+  const int32_t rows = 2 * G.g <= kMaxG ? 2 * G.g : G.g;  // room for look-ahead rows
+  return (size_t)n * G.Hkv * split * rows * (G.d + 2) * sizeof(float);
 }
 
 cudaError_t launch_attend(const Geom& G, const LayerState& S, const ReqTables& T, int32_t n_active,
-                          int32_t layer, const void* q, void* out, const CUtensorMap* pool_map,
-                          void* partials, Counters* ctr, int32_t* err, cudaStream_t s,
-                          int* n_launches, int* used_split) {
+                          int32_t layer, const void* q, void* out, const void* dq, void* dout,
+                          const CUtensorMap* pool_map, void* partials, int32_t* arrivals, Counters* ctr,
+                          int32_t* err, cudaStream_t s, int* n_launches, int* used_split) {
   *n_launches = 0;
   *used_split = 0;
   if (n_active <= 0) return cudaSuccess;
   cudaError_t e;
-  int32_t split;
-  if (use_mma(G)) {
-    const MmaShape sh = mma_shape();
-    split = pick_split(G, n_active, 2, sh.nw);
-    if (sh.nw == 8 && sh.ns == 2)
-      e = run_mma<8, 2>(G, S, T, n_active, layer, q, out, pool_map, partials, ctr, err, s, split);
-    else if (sh.nw == 8 && sh.ns == 3)
-      e = run_mma<8, 3>(G, S, T, n_active, layer, q, out, pool_map, partials, ctr, err, s, split);
-    else if (sh.ns == 2)
-      e = run_mma<4, 2>(G, S, T, n_active, layer, q, out, pool_map, partials, ctr, err, s, split);
-    else if (sh.ns == 4)
-      e = run_mma<4, 4>(G, S, T, n_active, layer, q, out, pool_map, partials, ctr, err, s, split);
-    else
-      e = run_mma<4, 3>(G, S, T, n_active, layer, q, out, pool_map, partials, ctr, err, s, split);
+  if (!dq || 2 * G.g <= kMaxG) {
+    // one pass: the draft heads (if any) ride in the MMA's spare columns next to the query heads
+    e = launch_rows(G, S, T, n_active, layer, q, dq, out, dout, dq ? 2 * G.g : G.g, pool_map, partials,
+                    arrivals, ctr, err, s, used_split);
+    if (e != cudaSuccess) return e;
+    *n_launches = 1;
   } else {
-    split = pick_split(G, n_active, 4, kSimtWarps);
-    const size_t smem = (size_t)(G.kb + 32) * 4 + (size_t)kSimtWarps * G.g * (G.d + 2) * 4;
-    const int grid = n_active * G.Hkv * split;
-    if (G.dtype == OKV_F32) {
-      e = cudaFuncSetAttribute(attend_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e == cudaSuccess)
-        attend_simt_kernel<float><<<grid, kSimtWarps * 32, smem, s>>>(
-            G, S, T, split, (const float*)q, (float*)out, (float*)partials, ctr, err);
-    } else {
-      e = cudaFuncSetAttribute(attend_simt_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e == cudaSuccess)
-        attend_simt_kernel<__nv_bfloat16><<<grid, kSimtWarps * 32, smem, s>>>(
-            G, S, T, split, (const __nv_bfloat16*)q, (__nv_bfloat16*)out, (float*)partials, ctr, err);
-    }
-    if (e == cudaSuccess) e = cudaGetLastError();
-  }
-  if (e != cudaSuccess) return e;
-  *n_launches = 1;
-  *used_split = split;
-  if (split > 1) {
-    if (G.dtype == OKV_F32)
-      combine_kernel<float><<<n_active * G.Hkv, 256, 0, s>>>(G, T, split, (const float*)partials, (float*)out);
-    else
-      combine_kernel<__nv_bfloat16><<<n_active * G.Hkv, 256, 0, s>>>(G, T, split, (const float*)partials,
-                                                                      (__nv_bfloat16*)out);
-    e = cudaGetLastError();
+    // a group too wide for both: two passes over the resident set
+    e = launch_rows(G, S, T, n_active, layer, q, nullptr, out, nullptr, G.g, pool_map, partials, arrivals,
+                    ctr, err, s, used_split);
+    if (e != cudaSuccess) return e;
+    e = launch_rows(G, S, T, n_active, layer, dq, nullptr, dout, nullptr, G.g, pool_map, partials, arrivals,
+                    ctr, err, s, used_split);
+    if (e != cudaSuccess) return e;
     *n_launches = 2;
   }
-  return e;
+  return cudaSuccess;
 }
 
 }  // namespace okv
@@ -656,7 +711,9 @@ namespace {
 constexpr size_t kStaticScratchBytes = (size_t)16 << 20;  // 16 MiB
 constexpr int32_t kStaticMaxRequests = 16384;
 constexpr size_t kStaticIdsOffset = 256;                  // [0, 256): error word, counters
-constexpr size_t kStaticPartialsOffset = kStaticIdsOffset + (size_t)kStaticMaxRequests * 4;
+constexpr int32_t kStaticMaxUnits = kStaticMaxRequests * 8;
+constexpr size_t kStaticArrivalsOffset = kStaticIdsOffset + (size_t)kStaticMaxRequests * 4;
+constexpr size_t kStaticPartialsOffset = kStaticArrivalsOffset + (size_t)kStaticMaxUnits * 4;
 
 static __device__ __align__(256) unsigned char okv_static_scratch[kStaticScratchBytes];
 
@@ -723,6 +780,7 @@ extern "C" okv_status okv_attend_static(int32_t n_requests, int32_t q_heads, int
                                         void* stream) {
   using namespace okv;
   if (n_requests <= 0 || n_requests > kStaticMaxRequests) return OKV_EINVAL;
+  if ((int64_t)n_requests * kv_heads > kStaticMaxUnits) return OKV_EINVAL;
   if (q_heads <= 0 || kv_heads <= 0 || q_heads % kv_heads || q_heads / kv_heads > kMaxG) return OKV_EINVAL;
   if (head_dim <= 0 || head_dim % 32 || head_dim > 256 || block_size <= 0 || block_size > 64) return OKV_EINVAL;
   if (slots <= 0 || slots > 1024 || (dtype != OKV_F32 && dtype != OKV_BF16)) return OKV_EINVAL;
@@ -769,9 +827,14 @@ extern "C" okv_status okv_attend_static(int32_t n_requests, int32_t q_heads, int
       return OKV_EINVAL;
     pmap = &map;
   }
+  // the split arrival counters must start at zero (the kernel leaves them at zero, but a call
+  // may follow any earlier one): clear them on the stream first
+  int32_t* arrivals = reinterpret_cast<int32_t*>(b + kStaticArrivalsOffset);
+  if (cudaMemsetAsync(arrivals, 0, (size_t)n_requests * kv_heads * 4, (cudaStream_t)stream) != cudaSuccess)
+    return OKV_ECUDA;
   int n_launch = 0, split = 0;
-  cudaError_t e = launch_attend(G, S, T, n_requests, 0, q, out, pmap, b + kStaticPartialsOffset,
-                                reinterpret_cast<Counters*>(b + 16), reinterpret_cast<int32_t*>(b),
+  cudaError_t e = launch_attend(G, S, T, n_requests, 0, q, out, nullptr, nullptr, pmap, b + kStaticPartialsOffset,
+                                arrivals, reinterpret_cast<Counters*>(b + 16), reinterpret_cast<int32_t*>(b),
                                 (cudaStream_t)stream, &n_launch, &split);
   return e == cudaSuccess ? OKV_OK : OKV_ECUDA;
 }

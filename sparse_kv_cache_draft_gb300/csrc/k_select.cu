@@ -64,26 +64,13 @@ __device__ __forceinline__ int32_t block_rank(bool flag, int32_t* scratch, int32
 constexpr int kScoreChunk = 128;
 
 template <typename T>
-__global__ void __launch_bounds__(kScoreThreads)
-score_kernel(Geom G, LayerState S, ReqTables RT, int32_t chunks, const T* __restrict__ draft,
-             uint32_t* __restrict__ ord_out, int32_t* err) {
+__device__ void score_chunk(const Geom& G, const LayerState& S, int32_t r, int32_t h, int32_t b_lo,
+                            int32_t b_hi, const T* __restrict__ draft, uint32_t* __restrict__ ord_out,
+                            float* coef) {
   constexpr int V = 16 / sizeof(T);
-  extern __shared__ __align__(16) uint8_t smem[];
-  float* coef = reinterpret_cast<float*>(smem);  // [2d]
-  const int32_t ua = blockIdx.x / chunks, chunk = blockIdx.x % chunks;
-  const int32_t a = ua / G.Hkv, h = ua % G.Hkv;
-  const int32_t r = RT.active[a];
   const int64_t unit = (int64_t)r * G.Hkv + h;
-  const int32_t len = S.len[r];
-  const int32_t nb = (len + G.bs - 1) / G.bs;
-  const int32_t b_lo = chunk * kScoreChunk;
-  if (len < 0 || nb > G.nb_max) {
-    if (threadIdx.x == 0 && chunk == 0) record_error(err, kErrLength, -1, r, len);
-    return;
-  }
-  if (b_lo >= nb) return;
-  const int32_t b_hi = min(nb, b_lo + kScoreChunk);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  __syncthreads();  // the shared buffer may hold the previous phase's data
   for (int32_t c = tid; c < G.d; c += blockDim.x) {
     float p = 0.f, n = 0.f;
     for (int32_t j = 0; j < G.g; ++j) {
@@ -138,6 +125,43 @@ score_kernel(Geom G, LayerState S, ReqTables RT, int32_t chunks, const T* __rest
   }
 }
 
+__device__ void select_unit(const Geom& G, const LayerState& S, int32_t r, int32_t h, int32_t nb_cap,
+                            int32_t kp2, const uint32_t* ord_in, int32_t cap_blocks, int32_t step,
+                            Counters* ctr, int32_t* err, uint8_t* smem, int32_t* pred_ids, int32_t* pred_n);
+
+// One CTA scores kScoreChunk blocks of one unit; the last of the unit's `chunks` CTAs to finish
+// (counted in `arrivals`, which it resets) then selects for the unit.
+template <typename T>
+__global__ void __launch_bounds__(kScoreThreads)
+stage_kernel(Geom G, LayerState S, ReqTables RT, int32_t chunks, int32_t nb_cap, int32_t kp2,
+             const T* __restrict__ draft, uint32_t* __restrict__ ord, int32_t* __restrict__ arrivals,
+             int32_t cap_blocks, int32_t step, Counters* ctr, int32_t* err, int32_t* pred_ids,
+             int32_t* pred_n) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ int32_t last;
+  const int32_t ua = blockIdx.x / chunks, chunk = blockIdx.x % chunks;
+  const int32_t a = ua / G.Hkv, h = ua % G.Hkv;
+  const int32_t r = RT.active[a];
+  const int32_t len = S.len[r];
+  const int32_t nb = (len + G.bs - 1) / G.bs;
+  const int32_t b_lo = chunk * kScoreChunk;
+  const bool bad = len < 0 || nb > G.nb_max || nb > nb_cap;
+  if (bad && threadIdx.x == 0 && chunk == 0) record_error(err, kErrLength, -1, r, len);
+  if (!bad && b_lo < nb)
+    score_chunk<T>(G, S, r, h, b_lo, min(nb, b_lo + kScoreChunk), draft, ord,
+                   reinterpret_cast<float*>(smem));
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    last = atomicAdd(&arrivals[ua], 1) == chunks - 1;
+    if (last) arrivals[ua] = 0;
+  }
+  __syncthreads();
+  if (!last || bad) return;
+  __threadfence();
+  select_unit(G, S, r, h, nb_cap, kp2, ord, cap_blocks, step, ctr, err, smem, pred_ids, pred_n);
+}
+
 // ---- top-K and diff / admit / evict, one CTA per unit -------------------------------------
 //
 // Top-K: a radix select over the order-preserving 32-bit score images finds the K-th largest
@@ -149,11 +173,11 @@ score_kernel(Geom G, LayerState S, ReqTables RT, int32_t chunks, const T* __rest
 // free slots by ascending slot, then unselected resident blocks by (stamp asc, block id asc);
 // each admitted block takes the target of its rank, the evicted block leaves the resident map,
 // and (block, slot) is appended to the fetch list.
-__global__ void __launch_bounds__(kScoreThreads)
-select_kernel(Geom G, LayerState S, ReqTables RT, int32_t nb_cap, int32_t kp2,
-              const uint32_t* __restrict__ ord_in, int32_t cap_blocks, int32_t step, Counters* ctr,
-              int32_t* err) {
-  extern __shared__ __align__(16) uint8_t smem[];
+// With pred_ids / pred_n set, only the top-K is computed and written there (prediction only:
+// the unit's selection, slot table and fetch list are left as they are).
+__device__ void select_unit(const Geom& G, const LayerState& S, int32_t r, int32_t h, int32_t nb_cap,
+                            int32_t kp2, const uint32_t* ord_in, int32_t cap_blocks, int32_t step,
+                            Counters* ctr, int32_t* err, uint8_t* smem, int32_t* pred_ids, int32_t* pred_n) {
   unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem);  // [kp2] selected keys
   unsigned long long* tkey = keys + kp2;                                   // [kb] eviction order
   uint32_t* ord = reinterpret_cast<uint32_t*>(tkey + G.kb);                // [nb_cap] score images
@@ -166,17 +190,13 @@ select_kernel(Geom G, LayerState S, ReqTables RT, int32_t nb_cap, int32_t kp2,
   int32_t* missrank = selid + G.kb;                                        // [kb] rank of a miss or -1
   int32_t* scratch = missrank + G.kb;                                      // [32 + 4]
 
-  const int32_t a = blockIdx.x / G.Hkv, h = blockIdx.x % G.Hkv;
-  const int32_t r = RT.active[a];
   const int64_t unit = (int64_t)r * G.Hkv + h;
   const int32_t len = S.len[r];
   const int32_t nb = (len + G.bs - 1) / G.bs;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (nb > nb_cap || nb > G.nb_max || len < 0) {
-    if (tid == 0) record_error(err, kErrLength, -1, r, len);
-    return;
-  }
-  for (int32_t b = tid; b < nb; b += blockDim.x) ord[b] = ord_in[unit * G.nb_max + b];
+  if (nb > nb_cap || nb > G.nb_max || len < 0) return;  // recorded by the scoring phase
+  // the scores were written by the other CTAs of this unit: read them past L1
+  for (int32_t b = tid; b < nb; b += blockDim.x) ord[b] = __ldcg(ord_in + unit * G.nb_max + b);
   __syncthreads();
 
   // ---- top-K: radix select of the K-th largest score image ----
@@ -258,6 +278,12 @@ select_kernel(Geom G, LayerState S, ReqTables RT, int32_t nb_cap, int32_t kp2,
       }
       __syncthreads();
     }
+  }
+  if (pred_ids) {
+    for (int32_t i = tid; i < K; i += blockDim.x)
+      pred_ids[unit * G.kb + i] = (int32_t)(~(uint32_t)(keys[i] & 0xFFFFFFFFull));
+    if (tid == 0) pred_n[unit] = K;
+    return;
   }
   for (int32_t i = tid; i < K; i += blockDim.x) {
     const unsigned long long k = keys[i];
@@ -349,30 +375,36 @@ select_kernel(Geom G, LayerState S, ReqTables RT, int32_t nb_cap, int32_t kp2,
 }  // namespace
 
 cudaError_t launch_stage(const Geom& G, const LayerState& S, const ReqTables& T, int32_t n_active,
-                         int32_t max_nb, const void* draft, uint32_t* scores, int32_t cap_blocks,
-                         int32_t step, Counters* ctr, int32_t* err, cudaStream_t s, int* n_launches) {
+                         int32_t max_nb, const void* draft, uint32_t* scores, int32_t* arrivals,
+                         int32_t cap_blocks, int32_t step, Counters* ctr, int32_t* err, cudaStream_t s,
+                         int* n_launches, int32_t* pred_ids, int32_t* pred_n) {
   *n_launches = 0;
   if (n_active <= 0) return cudaSuccess;
   const int32_t nb_cap = max_nb > 0 ? max_nb : 1;
   const int32_t chunks = (nb_cap + kScoreChunk - 1) / kScoreChunk;
-  const size_t smem_score = (size_t)2 * G.d * 4;
-  const int units = n_active * G.Hkv;
-  if (G.dtype == OKV_F32)
-    score_kernel<float><<<units * chunks, kScoreThreads, smem_score, s>>>(G, S, T, chunks, (const float*)draft,
-                                                                       scores, err);
-  else
-    score_kernel<__nv_bfloat16><<<units * chunks, kScoreThreads, smem_score, s>>>(
-        G, S, T, chunks, (const __nv_bfloat16*)draft, scores, err);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
   int32_t kp2 = 1;
   while (kp2 < G.kb) kp2 <<= 1;
-  const size_t smem = (size_t)(kp2 + G.kb) * 8 + (size_t)(nb_cap + 256) * 4 + (size_t)6 * G.kb * 4 + 36 * 4;
-  e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  select_kernel<<<units, kScoreThreads, smem, s>>>(G, S, T, nb_cap, kp2, scores, cap_blocks, step, ctr, err);
+  const size_t smem_select = (size_t)(kp2 + G.kb) * 8 + (size_t)(nb_cap + 256) * 4 + (size_t)6 * G.kb * 4 + 36 * 4;
+  const size_t smem_score = (size_t)2 * G.d * 4;
+  const size_t smem = smem_select > smem_score ? smem_select : smem_score;
+  const int grid = n_active * G.Hkv * chunks;
+  cudaError_t e;
+  if (G.dtype == OKV_F32) {
+    e = cudaFuncSetAttribute(stage_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    stage_kernel<float><<<grid, kScoreThreads, smem, s>>>(G, S, T, chunks, nb_cap, kp2, (const float*)draft,
+                                                          scores, arrivals, cap_blocks, step, ctr, err, pred_ids,
+                                                          pred_n);
+  } else {
+    e = cudaFuncSetAttribute(stage_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return e;
+    stage_kernel<__nv_bfloat16><<<grid, kScoreThreads, smem, s>>>(
+        G, S, T, chunks, nb_cap, kp2, (const __nv_bfloat16*)draft, scores, arrivals, cap_blocks, step, ctr, err,
+        pred_ids, pred_n);
+  }
   e = cudaGetLastError();
-  if (e == cudaSuccess) *n_launches = 2;
+  if (e == cudaSuccess) *n_launches = 1;
   return e;
 }
 

@@ -73,19 +73,27 @@ cudaError_t launch_reset_request(const Geom& G, int16_t* resident, int32_t* slot
                                  uint64_t* host_kv_tab, int32_t* cap_tab, cudaStream_t s);
 cudaError_t launch_advance(const LayerState& S, const ReqTables& T, int32_t n_active, cudaStream_t s);
 // Staging of one layer for every active unit: block scores (into `scores`, a [R][Hkv][nb_max]
-// uint32 workspace), then top-K and diff / admit / evict. Two launches.
+// uint32 workspace) by chunks of blocks; the last chunk of each unit to finish (counted in
+// `arrivals`, [R * Hkv] int32 that start at zero and are left at zero) runs the unit's top-K and
+// diff / admit / evict. One launch. With pred_ids / pred_n ([R][Hkv][Kb], [R][Hkv]) only the top-K
+// is computed, into them.
 cudaError_t launch_stage(const Geom& G, const LayerState& S, const ReqTables& T, int32_t n_active,
-                         int32_t max_nb, const void* draft, uint32_t* scores, int32_t cap_blocks,
-                         int32_t step, Counters* ctr, int32_t* err, cudaStream_t s, int* n_launches);
+                         int32_t max_nb, const void* draft, uint32_t* scores, int32_t* arrivals,
+                         int32_t cap_blocks, int32_t step, Counters* ctr, int32_t* err, cudaStream_t s,
+                         int* n_launches, int32_t* pred_ids = nullptr, int32_t* pred_n = nullptr);
 cudaError_t launch_gather(const Geom& G, const LayerState& S, const ReqTables& T, int32_t n_active,
                           int32_t layer, int32_t max_fetch, int32_t* err, cudaStream_t s);
 // Attention: decides between the tensor-core path (bf16, d = 128, g <= 8) and the CUDA-core
 // path; `partials` is a workspace of at least attend_workspace_bytes() bytes.
 size_t attend_workspace_bytes(const Geom& G, int32_t n_active);
+// `arrivals`: [n_active * Hkv] int32 split arrival counters that start at zero and are left at
+// zero; the last CTA of a split unit merges the partials.
+// With a draft query `dq` (look-ahead attention), its heads attend over the same resident set and
+// write `dout`: in the same pass when 2g <= 8, else in a second pass.
 cudaError_t launch_attend(const Geom& G, const LayerState& S, const ReqTables& T, int32_t n_active,
-                          int32_t layer, const void* q, void* out, const CUtensorMap* pool_map,
-                          void* partials, Counters* ctr, int32_t* err, cudaStream_t s,
-                          int* n_launches, int* used_split);
+                          int32_t layer, const void* q, void* out, const void* dq, void* dout,
+                          const CUtensorMap* pool_map, void* partials, int32_t* arrivals, Counters* ctr,
+                          int32_t* err, cudaStream_t s, int* n_launches, int* used_split);
 bool attend_uses_tensor_cores(const Geom& G);
 
 }  // namespace okv

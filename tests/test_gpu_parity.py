@@ -176,3 +176,66 @@ def test_api_errors():
     finally:
         ctx.close()
         hb.free()
+
+
+@pytest.mark.parametrize("name,w", [
+    ("qwen_bf16_one_pass", QWEN.scaled(layers=1, batch=3)),
+    ("gqa8_two_passes", synth.WORKLOADS["gqa32b_32k_b32"].scaled(layers=1, batch=2)),
+    ("tiny_fp32_one_pass", synth.WORKLOADS["tiny"]),
+])
+def test_lookahead_attention(name, w):
+    """Normal and draft queries attend together over the resident set."""
+    import torch
+    from okv_harness import torch_dtype
+    rig = Rig(w)
+    try:
+        rig.stage(0, 0, 1.0, draft_step=-1)
+        rig.stage(0, 1, w.fetch_cap, draft_step=0)
+        shp = (rig.R, w.q_heads, w.head_dim)
+        q = rig.batch_queries(0, 1, 0)
+        dq = rig.batch_queries(0, 1, 1)
+        out = torch.zeros(shp, dtype=torch_dtype(w.dtype), device="cuda")
+        dout = torch.zeros(shp, dtype=torch_dtype(w.dtype), device="cuda")
+        rig.ctx.attend_lookahead(0, rig.device_rows(q, shp[1:]), rig.device_rows(dq, shp[1:]), out, dout)
+        torch.cuda.synchronize()
+        assert rig.check_attention(0, q, out) <= ATOL[w.dtype]
+        assert rig.check_attention(0, dq, dout) <= ATOL[w.dtype]
+    finally:
+        rig.close()
+
+
+def test_predict_matches_oracle_topk():
+    """okv_predict: top-K of any query (here the true next query) equals the oracle's, within the
+    tie band, and leaves the context's own selection untouched."""
+    import torch
+    import oracle as O
+    from okv_harness import TIE_REL
+    w = QWEN.scaled(layers=1, batch=3)
+    rig = Rig(w)
+    try:
+        rig.stage(0, 0, 1.0, draft_step=-1)
+        before = rig.ctx.read_selection(0)
+        q = rig.batch_queries(0, 1, 0)
+        counts = torch.zeros((rig.R, w.kv_heads), dtype=torch.int32, device="cuda")
+        ids = torch.full((rig.R, w.kv_heads, rig.kb), -1, dtype=torch.int32, device="cuda")
+        rig.ctx.predict(0, rig.device_rows(q, (w.q_heads, w.head_dim)), counts, ids)
+        torch.cuda.synchronize()
+        counts, ids = counts.cpu().numpy(), ids.cpu().numpy()
+        g = w.group
+        for i in range(w.batch):
+            nb = -(-int(rig.model.n_tok[0, i]) // w.block_size)
+            for h in range(w.kv_heads):
+                osc = O.block_scores(np.ascontiguousarray(rig.model.summ[0][i, h, :nb]), q[i, h * g:(h + 1) * g])
+                osel = O.topk(osc, rig.kb)
+                n = len(osel)
+                assert counts[i, h] == n
+                gsel = ids[i, h, :n]
+                diff = set(gsel.tolist()) ^ set(osel.tolist())
+                if diff:
+                    sK = float(osc[osel[-1]])
+                    band = set(np.nonzero(np.abs(osc.astype(np.float64) - sK) <= TIE_REL * abs(sK))[0].tolist())
+                    assert diff <= band, (i, h, sorted(diff - band))
+        after = rig.ctx.read_selection(0)
+        assert all(np.array_equal(a, b) for a, b in zip(before, after))
+    finally:
+        rig.close()
