@@ -57,9 +57,10 @@ def parse_args():
     p.add_argument("--batch", type=int, default=0, help="override the batch (smaller profiling cases)")
     p.add_argument("--layers", type=int, default=0, help="override the layer count (smaller profiling cases)")
     p.add_argument("--baseline-layers", type=int, default=6, help="layers in the cpu_baseline sample")
-    p.add_argument("--report", choices=["bench", "capsweep", "agreement"], default="bench",
+    p.add_argument("--report", choices=["bench", "capsweep", "agreement", "dense"], default="bench",
                    help="capsweep: bytes per step and tok/s per fetch cap (batch-90 sweep workload); "
-                        "agreement: draft vs previous-token top-K agreement with the true next query")
+                        "agreement: draft vs previous-token top-K agreement with the true next query; "
+                        "dense: dense decode attention over the full KV in HBM vs the sparse path, same shapes")
     p.add_argument("--workload", default=None, help="synthetic workload name (default: the metric's)")
     return p.parse_args()
 
@@ -577,6 +578,78 @@ def run_agreement(args, dist: Dist):
             "proxy_per_layer": [round(float(x), 4) for x in proxy_agree.mean(0)]}
 
 
+def run_dense(args, dist: Dist):
+    """Dense decode attention over the full KV held in HBM (the attention kernel over an identity slot
+    table of every block) against the sparse path at the same shapes and batch."""
+    import numpy as np
+    import torch
+    from sparse_kv_cache_draft_gb300 import BF16, binding
+    wl = Workload(args.alias, args.threads, args.batch or 64, args.layers, args.workload)
+    bufs = wl.host_kv()
+    K, W = args.steps, args.warmup
+    L, B, Hkv, nb, d = wl.L, wl.B, wl.Hkv, wl.nb, wl.d
+    bs = wl.w.block_size
+    unit_bytes = nb * 2 * bs * d * 2
+    kv = torch.empty((L, B, Hkv, nb, 2, bs, d), dtype=torch.bfloat16, device="cuda")
+    for k, b in enumerate(bufs):
+        host = torch.from_numpy(b.numpy(np.int16, (L, Hkv, nb, 2, bs, d))).view(torch.bfloat16)
+        for r in range(B):
+            if int(wl.keys[r]) == k:
+                for l in range(L):
+                    kv[l, r].copy_(host[l])
+    sb = torch.arange(nb, dtype=torch.int32, device="cuda").repeat(B, Hkv, 1).contiguous()
+    lens = torch.full((B,), wl.n_tok, dtype=torch.int32, device="cuda")
+    q, dr = _device_inputs(wl, W + K)
+    out = torch.empty(q.shape[1:], dtype=torch.bfloat16, device="cuda")
+
+    def dense_step(t):
+        for l in range(L):
+            binding.attend_static(kv[l], sb, lens, q[t, l], out[l], q_heads=wl.Hq, kv_heads=Hkv, head_dim=d,
+                                  block_size=bs, slots=nb, dtype=BF16)
+
+    for t in range(W):
+        dense_step(t)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for t in range(W, W + K):
+        dense_step(t)
+    e1.record()
+    e1.synchronize()
+    dense_ms = dist.max(e0.elapsed_time(e1))
+    del kv
+    torch.cuda.empty_cache()
+    # the sparse path at the same batch
+    ctx = _setup_context(wl, bufs)
+    for l in range(L):
+        ctx.stage(l, dr[0, l], 0, 1.0)
+    for t in range(W):
+        ctx.step(q[t], dr[t + 1], out, t + 1)
+    torch.cuda.synchronize()
+    e0.record()
+    for t in range(W, W + K):
+        ctx.step(q[t], dr[t + 1], out, t + 1)
+    ctx.join()
+    e1.record()
+    e1.synchronize()
+    sparse_ms = dist.max(e0.elapsed_time(e1))
+    ctx.close()
+    for b in bufs:
+        b.free()
+    dense_tok = dist.world * B * K / (dense_ms / 1e3)
+    sparse_tok = dist.world * B * K / (sparse_ms / 1e3)
+    hbm_peak, src = measured_peaks()
+    dense_bytes = L * B * Hkv * unit_bytes
+    return {"report": "dense", "metric": "decode attention tok/s, dense (full KV in HBM) vs sparse staging",
+            "unit": "tok/s", "n_gpus": dist.world, "steps": K, "warmup": W, "data": "synthetic",
+            "config": wl.config_json(), "dense_tok_s": round(dense_tok, 1), "sparse_tok_s": round(sparse_tok, 1),
+            "sparse_over_dense": round(sparse_tok / dense_tok, 3),
+            "dense_ms_per_step": round(dense_ms / K, 3), "sparse_ms_per_step": round(sparse_ms / K, 3),
+            "dense_hbm_gbs": round(dense_bytes / (dense_ms / K / 1e3) / 1e9, 1),
+            "dense_hbm_frac": round(dense_bytes / (dense_ms / K / 1e3) / 1e9 / hbm_peak, 4),
+            "peak_source": f"hbm_gbs, {src}"}
+
+
 def main():
     args = parse_args()
     dist = Dist(want_gpu=args.impl == "okv")
@@ -585,6 +658,8 @@ def main():
             res = run_capsweep(args, dist) if dist.rank == 0 else None
         elif args.report == "agreement":
             res = run_agreement(args, dist) if dist.rank == 0 else None
+        elif args.report == "dense":
+            res = run_dense(args, dist) if dist.rank == 0 else None
         else:
             res = run_okv(args, dist) if args.impl == "okv" else run_reference(args, dist)
         if res is not None and dist.rank == 0:
