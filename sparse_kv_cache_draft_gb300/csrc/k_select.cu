@@ -85,6 +85,48 @@ __device__ void score_chunk(const Geom& G, const LayerState& S, int32_t r, int32
   const int32_t nvec = 2 * G.d / V;  // 16-byte vectors per summary record
   const T* summ = reinterpret_cast<const T*>(S.summ) + unit * G.nb_max * 2 * G.d;
   uint32_t* ord = ord_out + unit * G.nb_max;
+  if (nvec <= 32) {
+    // one vector per lane (bf16 up to d = 128, fp32 up to d = 64): the lane's coefficients stay
+    // in registers and each warp keeps 8 blocks of loads in flight
+    constexpr int U = 8;
+    float cf[V];
+#pragma unroll
+    for (int e = 0; e < V; ++e) cf[e] = lane < nvec ? coef[lane * V + e] : 0.f;
+    for (int32_t b0 = b_lo + warp * U; b0 < b_hi; b0 += nwarps * U) {
+      union {
+        uint4 u4;
+        T e[V];
+      } x[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int32_t b = b0 + u;
+        x[u].u4 = (b < b_hi && lane < nvec)
+                      ? __ldcs(reinterpret_cast<const uint4*>(summ + (int64_t)b * 2 * G.d) + lane)
+                      : make_uint4(0, 0, 0, 0);
+      }
+      float part[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < V; ++e) acc = fmaf(cf[e], to_f(x[u].e[e]), acc);
+        part[u] = acc;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) part[u] += __shfl_xor_sync(0xffffffffu, part[u], o);
+      }
+      if (lane < U) {
+        float sc = part[0];
+#pragma unroll
+        for (int u = 1; u < U; ++u)
+          if (lane == u) sc = part[u];
+        if (b0 + lane < b_hi) ord[b0 + lane] = orderable(sc);
+      }
+    }
+    return;
+  }
   constexpr int U = 4;  // blocks in flight per warp
   for (int32_t b0 = b_lo + warp * U; b0 < b_hi; b0 += nwarps * U) {
     float part[U];

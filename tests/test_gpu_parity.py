@@ -239,3 +239,19 @@ def test_predict_matches_oracle_topk():
         assert all(np.array_equal(a, b) for a, b in zip(before, after))
     finally:
         rig.close()
+
+
+@pytest.mark.parametrize("cap", [0.01, 0.02, 0.1, 0.25])
+def test_capsweep_workload(cap):
+    """The fetch-cap sweep workload (100 directions, 5 active, one replaced per step) at each cap:
+    C = 1, 2, 12, 32 blocks per unit and step, state carried over 3 steps."""
+    import oracle as O
+    w = synth.WORKLOADS["qwen3_8b_capsweep_b90"].scaled(layers=1, batch=3)
+    rig = Rig(w)
+    try:
+        errs, _ = rig.run_steps(3, cap)
+        assert max(errs) <= ATOL[BF16]
+        counts, _ = rig.ctx.read_fetch_list(0)
+        assert counts[:3].max() <= O.fetch_cap_blocks(cap, rig.kb)
+    finally:
+        rig.close()
