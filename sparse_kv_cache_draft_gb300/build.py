@@ -36,7 +36,8 @@ def _flags(verbose: bool):
 def _stale(obj: str, src: str) -> bool:
     if not os.path.exists(obj):
         return True
-    deps = [src, os.path.join(CSRC, "okv_internal.h"), os.path.join(HERE, "..", "include", "okv.h")]
+    deps = [src, os.path.join(HERE, "..", "include", "okv.h")] + [
+        os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
     return any(os.path.getmtime(d) > os.path.getmtime(obj) for d in deps)
 
 

@@ -7,20 +7,10 @@
 #include <cuda_bf16.h>
 
 #include "okv_internal.h"
+#include "ptx.cuh"
 
 namespace okv {
 namespace {
-
-constexpr int kScoreThreads = 256;
-
-__device__ __forceinline__ void record_error(int32_t* err, int32_t code, int32_t a, int32_t b,
-                                             int32_t c) {
-  if (atomicCAS(err, 0, code) == 0) {
-    err[1] = a;
-    err[2] = b;
-    err[3] = c;
-  }
-}
 
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
@@ -57,11 +47,17 @@ __device__ __forceinline__ int32_t block_rank(bool flag, int32_t* scratch, int32
 //
 // Score of block b for KV head h: sum over the g query heads of the group of
 // sum_c max(q_c kmin_c, q_c kmax_c) = sum_c (P_c kmax_c + N_c kmin_c), P_c (N_c) being the sum
-// of the group's positive (negative) query coordinates. One CTA scores kScoreChunk blocks of
-// one unit; each warp reads one 16-byte vector per lane of a block's [kmin | kmax] record (2d
-// elements), multiplies by the matching N or P coefficient and reduces across the warp. The
-// order-preserving 32-bit image of each binary32 score goes to `ord`.
+// of the group's positive (negative) query coordinates. One CTA scores up to kScoreChunk blocks
+// of one unit: each warp takes 8 blocks at a time, one 16-byte load per lane per block of the
+// block's [kmin | kmax] record (2d elements) with the lane's coefficients in registers, and
+// reduces the 8 block sums across the warp. The order-preserving 32-bit image of each
+// binary32 score goes to `ord_out`. (Staging the chunk through shared memory with one bulk TMA
+// copy was measured slower: its 64 KiB buffer leaves 3 scoring CTAs per SM and the selection
+// tails hold them.)
 constexpr int kScoreChunk = 128;
+constexpr int kStageThreads = 256;
+
+__host__ __device__ inline size_t coef_bytes(const Geom& G) { return ((size_t)2 * G.d * 4 + 15) & ~size_t(15); }
 
 template <typename T>
 __device__ void score_chunk(const Geom& G, const LayerState& S, int32_t r, int32_t h, int32_t b_lo,
@@ -70,7 +66,6 @@ __device__ void score_chunk(const Geom& G, const LayerState& S, int32_t r, int32
   constexpr int V = 16 / sizeof(T);
   const int64_t unit = (int64_t)r * G.Hkv + h;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-  __syncthreads();  // the shared buffer may hold the previous phase's data
   for (int32_t c = tid; c < G.d; c += blockDim.x) {
     float p = 0.f, n = 0.f;
     for (int32_t j = 0; j < G.g; ++j) {
@@ -86,8 +81,8 @@ __device__ void score_chunk(const Geom& G, const LayerState& S, int32_t r, int32
   const T* summ = reinterpret_cast<const T*>(S.summ) + unit * G.nb_max * 2 * G.d;
   uint32_t* ord = ord_out + unit * G.nb_max;
   if (nvec <= 32) {
-    // one vector per lane (bf16 up to d = 128, fp32 up to d = 64): the lane's coefficients stay
-    // in registers and each warp keeps 8 blocks of loads in flight
+    // one vector per lane (bf16 up to d = 128, fp32 up to d = 64): coefficients in registers,
+    // 8 blocks of loads in flight per warp
     constexpr int U = 8;
     float cf[V];
 #pragma unroll
@@ -104,144 +99,117 @@ __device__ void score_chunk(const Geom& G, const LayerState& S, int32_t r, int32
                       ? __ldcs(reinterpret_cast<const uint4*>(summ + (int64_t)b * 2 * G.d) + lane)
                       : make_uint4(0, 0, 0, 0);
       }
-      float part[U];
+      float p8[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         float acc = 0.f;
 #pragma unroll
         for (int e = 0; e < V; ++e) acc = fmaf(cf[e], to_f(x[u].e[e]), acc);
-        part[u] = acc;
+        p8[u] = acc;
       }
+      // transposing butterfly: each exchange halves the values a lane carries, so the 8 block
+      // sums take 9 shuffles; lane quad q ends with the sum of block (bit4, bit3, bit2 of lane)
+      float p4[4], p2[2];
+      const bool b16 = lane & 16, b8 = lane & 8, b4 = lane & 4;
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
+      for (int i = 0; i < 4; ++i)
+        p4[i] = (b16 ? p8[i + 4] : p8[i]) + __shfl_xor_sync(0xffffffffu, b16 ? p8[i] : p8[i + 4], 16);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) part[u] += __shfl_xor_sync(0xffffffffu, part[u], o);
-      }
-      if (lane < U) {
-        float sc = part[0];
-#pragma unroll
-        for (int u = 1; u < U; ++u)
-          if (lane == u) sc = part[u];
-        if (b0 + lane < b_hi) ord[b0 + lane] = orderable(sc);
-      }
+      for (int i = 0; i < 2; ++i)
+        p2[i] = (b8 ? p4[i + 2] : p4[i]) + __shfl_xor_sync(0xffffffffu, b8 ? p4[i] : p4[i + 2], 8);
+      float sc = (b4 ? p2[1] : p2[0]) + __shfl_xor_sync(0xffffffffu, b4 ? p2[0] : p2[1], 4);
+      sc += __shfl_xor_sync(0xffffffffu, sc, 2);
+      sc += __shfl_xor_sync(0xffffffffu, sc, 1);
+      const int32_t b = b0 + (b16 ? 4 : 0) + (b8 ? 2 : 0) + (b4 ? 1 : 0);
+      if ((lane & 3) == 0 && b < b_hi) ord[b] = orderable(sc);
     }
     return;
   }
-  constexpr int U = 4;  // blocks in flight per warp
-  for (int32_t b0 = b_lo + warp * U; b0 < b_hi; b0 += nwarps * U) {
-    float part[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) part[u] = 0.f;
+  for (int32_t b = b_lo + warp; b < b_hi; b += nwarps) {
+    float part = 0.f;
     for (int32_t v = lane; v < nvec; v += 32) {
       union {
         uint4 u4;
         T e[V];
-      } x[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int32_t b = b0 + u;
-        x[u].u4 = b < b_hi ? __ldcs(reinterpret_cast<const uint4*>(summ + (int64_t)b * 2 * G.d) + v)
-                           : make_uint4(0, 0, 0, 0);
-      }
+      } x;
+      x.u4 = __ldcs(reinterpret_cast<const uint4*>(summ + (int64_t)b * 2 * G.d) + v);
       const float* cf = coef + v * V;
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        float acc = 0.f;
-#pragma unroll
-        for (int e = 0; e < V; ++e) acc = fmaf(cf[e], to_f(x[u].e[e]), acc);
-        part[u] += acc;
-      }
+      for (int e = 0; e < V; ++e) part = fmaf(cf[e], to_f(x.e[e]), part);
     }
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) part[u] += __shfl_xor_sync(0xffffffffu, part[u], o);
-    }
-    if (lane < U) {
-      float sc = part[0];
-#pragma unroll
-      for (int u = 1; u < U; ++u)
-        if (lane == u) sc = part[u];
-      if (b0 + lane < b_hi) ord[b0 + lane] = orderable(sc);
-    }
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (lane == 0) ord[b] = orderable(part);
   }
 }
 
-__device__ void select_unit(const Geom& G, const LayerState& S, int32_t r, int32_t h, int32_t nb_cap,
-                            int32_t kp2, const uint32_t* ord_in, int32_t cap_blocks, int32_t step,
-                            Counters* ctr, int32_t* err, uint8_t* smem, int32_t* pred_ids, int32_t* pred_n);
-
-// One CTA scores kScoreChunk blocks of one unit; the last of the unit's `chunks` CTAs to finish
-// (counted in `arrivals`, which it resets) then selects for the unit.
-template <typename T>
-__global__ void __launch_bounds__(kScoreThreads)
-stage_kernel(Geom G, LayerState S, ReqTables RT, int32_t chunks, int32_t nb_cap, int32_t kp2,
-             const T* __restrict__ draft, uint32_t* __restrict__ ord, int32_t* __restrict__ arrivals,
-             int32_t cap_blocks, int32_t step, Counters* ctr, int32_t* err, int32_t* pred_ids,
-             int32_t* pred_n) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  __shared__ int32_t last;
-  const int32_t ua = blockIdx.x / chunks, chunk = blockIdx.x % chunks;
-  const int32_t a = ua / G.Hkv, h = ua % G.Hkv;
-  const int32_t r = RT.active[a];
-  const int32_t len = S.len[r];
-  const int32_t nb = (len + G.bs - 1) / G.bs;
-  const int32_t b_lo = chunk * kScoreChunk;
-  const bool bad = len < 0 || nb > G.nb_max || nb > nb_cap;
-  if (bad && threadIdx.x == 0 && chunk == 0) record_error(err, kErrLength, -1, r, len);
-  if (!bad && b_lo < nb)
-    score_chunk<T>(G, S, r, h, b_lo, min(nb, b_lo + kScoreChunk), draft, ord,
-                   reinterpret_cast<float*>(smem));
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    last = atomicAdd(&arrivals[ua], 1) == chunks - 1;
-    if (last) arrivals[ua] = 0;
-  }
-  __syncthreads();
-  if (!last || bad) return;
-  __threadfence();
-  select_unit(G, S, r, h, nb_cap, kp2, ord, cap_blocks, step, ctr, err, smem, pred_ids, pred_n);
-}
-
-// ---- top-K and diff / admit / evict, one CTA per unit -------------------------------------
+// ---- top-K and diff / admit / evict (one unit) ---------------------------------------------
 //
-// Top-K: a radix select over the order-preserving 32-bit score images finds the K-th largest
-// score T; blocks above T are selected, and of the blocks equal to T the lowest ids fill the
-// rest. The K selected (score, ~id) keys are then sorted, descending.
+// Top-K: a radix select over the order-preserving score images finds the K-th largest image T;
+// the blocks at or above T are sorted by (score desc, block id asc) and the first K are the
+// selection (equal scores resolve to the lower block id).
 //
-// Diff / admit / evict: hits (selected and resident) keep their slot and get stamp = step;
-// misses are ranked in selection order and the first min(C, #misses) are admitted; targets are
-// free slots by ascending slot, then unselected resident blocks by (stamp asc, block id asc);
-// each admitted block takes the target of its rank, the evicted block leaves the resident map,
-// and (block, slot) is appended to the fetch list.
+// Diff / admit / evict: a block -> slot map of the unit's slot table is built in shared memory;
+// hits (selected and resident) keep their slot and get stamp = step; misses are ranked in
+// selection order and the first min(C, #misses) are admitted; targets are free slots by
+// ascending slot, then unselected resident blocks by (stamp asc, block id asc); each admitted
+// block takes the target of its rank and (block, slot) is appended to the fetch list.
+//
 // With pred_ids / pred_n set, only the top-K is computed and written there (prediction only:
 // the unit's selection, slot table and fetch list are left as they are).
-__device__ void select_unit(const Geom& G, const LayerState& S, int32_t r, int32_t h, int32_t nb_cap,
-                            int32_t kp2, const uint32_t* ord_in, int32_t cap_blocks, int32_t step,
+__host__ __device__ inline size_t pow2_at_least(size_t n) {
+  size_t p = 2;
+  while (p < n) p <<= 1;
+  return p;
+}
+
+__host__ __device__ inline size_t select_bytes(const Geom& G, int32_t nb_cap) {
+  const size_t kp = pow2_at_least((size_t)nb_cap > (size_t)G.kb ? (size_t)nb_cap : (size_t)G.kb);
+  return kp * 8 + (size_t)G.kb * 8 + (size_t)nb_cap * 4 + 256 * 4 + (((size_t)nb_cap * 2 + 15) & ~size_t(15)) +
+         (size_t)6 * G.kb * 4 + 40 * 4;
+}
+
+__device__ void select_unit(const Geom& G, const LayerState& S, int32_t r, int32_t h, int32_t nb,
+                            int32_t nb_cap, const uint32_t* ord_in, int32_t cap_blocks, int32_t step,
                             Counters* ctr, int32_t* err, uint8_t* smem, int32_t* pred_ids, int32_t* pred_n) {
-  unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem);  // [kp2] selected keys
-  unsigned long long* tkey = keys + kp2;                                   // [kb] eviction order
+  const size_t kp = pow2_at_least((size_t)nb_cap > (size_t)G.kb ? (size_t)nb_cap : (size_t)G.kb);
+  unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem);  // [kp] candidates
+  unsigned long long* tkey = keys + kp;                                    // [kb] eviction order
   uint32_t* ord = reinterpret_cast<uint32_t*>(tkey + G.kb);                // [nb_cap] score images
   uint32_t* hist = ord + nb_cap;                                           // [256]
-  int32_t* sb = reinterpret_cast<int32_t*>(hist + 256);                    // [kb] slot -> block
-  int32_t* st = sb + G.kb;                                                 // [kb] stamps
-  int32_t* hit = st + G.kb;                                                // [kb]
-  int32_t* target = hit + G.kb;                                            // [kb]
-  int32_t* selid = target + G.kb;                                          // [kb] selection, in order
-  int32_t* missrank = selid + G.kb;                                        // [kb] rank of a miss or -1
-  int32_t* scratch = missrank + G.kb;                                      // [32 + 4]
+  int16_t* b2s = reinterpret_cast<int16_t*>(hist + 256);                   // [nb_cap] block -> slot
+  int32_t* sb = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(b2s) + (((size_t)nb_cap * 2 + 15) & ~size_t(15)));
+  int32_t* st = sb + G.kb;        // [kb] stamps
+  int32_t* hit = st + G.kb;       // [kb]
+  int32_t* target = hit + G.kb;   // [kb]
+  int32_t* selid = target + G.kb; // [kb] selection, in order
+  int32_t* missrank = selid + G.kb;  // [kb] rank of a miss, or -1
+  int32_t* scratch = missrank + G.kb;  // [40]
 
   const int64_t unit = (int64_t)r * G.Hkv + h;
-  const int32_t len = S.len[r];
-  const int32_t nb = (len + G.bs - 1) / G.bs;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (nb > nb_cap || nb > G.nb_max || len < 0) return;  // recorded by the scoring phase
+  const bool predict = pred_ids != nullptr;
   // the scores were written by the other CTAs of this unit: read them past L1
-  for (int32_t b = tid; b < nb; b += blockDim.x) ord[b] = __ldcg(ord_in + unit * G.nb_max + b);
+  for (int32_t b = tid; b < nb; b += blockDim.x) {
+    ord[b] = __ldcg(ord_in + unit * G.nb_max + b);
+    b2s[b] = -1;
+  }
+  if (!predict)
+    for (int32_t s = tid; s < G.kb; s += blockDim.x) {
+      sb[s] = S.slot_block[unit * G.kb + s];
+      st[s] = S.stamp[unit * G.kb + s];
+      hit[s] = 0;
+    }
+  if (tid == 0) scratch[34] = 0;
   __syncthreads();
+  if (!predict)
+    for (int32_t s = tid; s < G.kb; s += blockDim.x) {
+      const int32_t b = sb[s];
+      if (b >= nb) record_error(err, kErrBlockRange, -1, r, b);
+      else if (b >= 0) b2s[b] = (int16_t)s;
+    }
 
-  // ---- top-K: radix select of the K-th largest score image ----
+  // ---- top-K: radix select of the K-th largest score image T ----
   const int32_t K = nb < G.kb ? nb : G.kb;
   uint32_t prefix = 0, mask = 0;
   int32_t krem = K;
@@ -289,26 +257,22 @@ __device__ void select_unit(const Geom& G, const LayerState& S, int32_t r, int32
       __syncthreads();
     }
   }
-  // prefix = K-th largest image T (K < nb); krem = how many blocks equal to T are taken
-  int32_t base_eq = 0, base_sel = 0;
-  for (int32_t b0 = 0; b0 < nb; b0 += blockDim.x) {
-    const int32_t b = b0 + tid;
-    const uint32_t u = b < nb ? ord[b] : 0u;
-    const bool eq = K < nb && b < nb && u == prefix;
-    int32_t n_eq;
-    const int32_t eqr = base_eq + block_rank(eq, scratch, &n_eq);
-    const bool take = b < nb && (K >= nb || u > prefix || (eq && eqr < krem));
-    int32_t n_take;
-    const int32_t pos = base_sel + block_rank(take, scratch, &n_take);
-    if (take) keys[pos] = ((unsigned long long)u << 32) | (unsigned long long)(~(uint32_t)b);
-    base_eq += n_eq;
-    base_sel += n_take;
+  // candidates: every block at or above T (all of them when the budget covers the context)
+  for (int32_t b = tid; b < nb; b += blockDim.x) {
+    const uint32_t u = ord[b];
+    if (K >= nb || u >= prefix) {
+      const int32_t pos = atomicAdd(&scratch[34], 1);
+      keys[pos] = ((unsigned long long)u << 32) | (unsigned long long)(~(uint32_t)b);
+    }
   }
-  for (int32_t i = K + tid; i < kp2; i += blockDim.x) keys[i] = 0ull;
   __syncthreads();
-  for (int32_t k = 2; k <= kp2; k <<= 1) {  // bitonic sort, descending
+  const int32_t n_cand = scratch[34];
+  const int32_t cp = (int32_t)pow2_at_least((size_t)n_cand);
+  for (int32_t i = n_cand + tid; i < cp; i += blockDim.x) keys[i] = 0ull;
+  __syncthreads();
+  for (int32_t k = 2; k <= cp; k <<= 1) {  // bitonic sort, descending
     for (int32_t j = k >> 1; j > 0; j >>= 1) {
-      for (int32_t i = tid; i < kp2; i += blockDim.x) {
+      for (int32_t i = tid; i < cp; i += blockDim.x) {
         const int32_t ixj = i ^ j;
         if (ixj > i) {
           const unsigned long long x = keys[i], y = keys[ixj];
@@ -321,7 +285,7 @@ __device__ void select_unit(const Geom& G, const LayerState& S, int32_t r, int32
       __syncthreads();
     }
   }
-  if (pred_ids) {
+  if (predict) {
     for (int32_t i = tid; i < K; i += blockDim.x)
       pred_ids[unit * G.kb + i] = (int32_t)(~(uint32_t)(keys[i] & 0xFFFFFFFFull));
     if (tid == 0) pred_n[unit] = K;
@@ -333,31 +297,19 @@ __device__ void select_unit(const Geom& G, const LayerState& S, int32_t r, int32
     selid[i] = b;
     S.sel_ids[unit * G.kb + i] = b;
     S.sel_scores[unit * G.kb + i] = from_orderable((uint32_t)(k >> 32));
-  }
-  if (tid == 0) S.n_sel[unit] = K;
-
-  // ---- diff / admit / evict ----
-  int16_t* resident = S.resident + unit * G.nb_max;
-  for (int32_t s = tid; s < G.kb; s += blockDim.x) {
-    sb[s] = S.slot_block[unit * G.kb + s];
-    st[s] = S.stamp[unit * G.kb + s];
-    hit[s] = 0;
-  }
-  __syncthreads();
-  for (int32_t i = tid; i < K; i += blockDim.x) {
-    const int32_t b = selid[i];
-    const int32_t s = resident[b];
-    missrank[i] = -1;
-    if (s >= G.kb) {
-      record_error(err, kErrSlotRange, -1, r, s);
-    } else if (s >= 0) {
+    const int32_t s = b2s[b];
+    if (s >= 0) {
       hit[s] = 1;
       st[s] = step;
+      missrank[i] = -1;
     } else {
       missrank[i] = 0;
     }
   }
+  if (tid == 0) S.n_sel[unit] = K;
   __syncthreads();
+
+  // ---- diff / admit / evict ----
   int32_t n_miss = 0;
   for (int32_t i0 = 0; i0 < K; i0 += blockDim.x) {
     const int32_t i = i0 + tid;
@@ -395,9 +347,6 @@ __device__ void select_unit(const Geom& G, const LayerState& S, int32_t r, int32
     if (rk < 0 || rk >= n_admit) continue;
     const int32_t b = selid[i];
     const int32_t s = target[rk];
-    const int32_t old = sb[s];
-    if (old >= 0) resident[old] = -1;
-    resident[b] = (int16_t)s;
     sb[s] = b;
     st[s] = step;
     S.fetch[(unit * G.kb + rk) * 2 + 0] = b;
@@ -414,6 +363,38 @@ __device__ void select_unit(const Geom& G, const LayerState& S, int32_t r, int32
   }
 }
 
+// One CTA scores kScoreChunk blocks of one unit; the last of the unit's `chunks` CTAs to finish
+// (counted in `arrivals`, which it resets) then selects for the unit.
+template <typename T>
+__global__ void __launch_bounds__(kStageThreads)
+stage_kernel(Geom G, LayerState S, ReqTables RT, int32_t chunks, int32_t nb_cap,
+             const T* __restrict__ draft, uint32_t* __restrict__ ord, int32_t* __restrict__ arrivals,
+             int32_t cap_blocks, int32_t step, Counters* ctr, int32_t* err, int32_t* pred_ids,
+             int32_t* pred_n) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ int32_t last;
+  const int32_t ua = blockIdx.x / chunks, chunk = blockIdx.x % chunks;
+  const int32_t a = ua / G.Hkv, h = ua % G.Hkv;
+  const int32_t r = RT.active[a];
+  const int32_t len = S.len[r];
+  const int32_t nb = (len + G.bs - 1) / G.bs;
+  const int32_t b_lo = chunk * kScoreChunk;
+  const bool bad = len < 0 || nb > G.nb_max || nb > nb_cap;
+  if (bad && threadIdx.x == 0 && chunk == 0) record_error(err, kErrLength, -1, r, len);
+  if (!bad && b_lo < nb)
+    score_chunk<T>(G, S, r, h, b_lo, min(nb, b_lo + kScoreChunk), draft, ord, reinterpret_cast<float*>(smem + 16));
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    last = atomicAdd(&arrivals[ua], 1) == chunks - 1;
+    if (last) arrivals[ua] = 0;
+  }
+  __syncthreads();
+  if (!last || bad) return;
+  __threadfence();
+  select_unit(G, S, r, h, nb, nb_cap, ord, cap_blocks, step, ctr, err, smem + 16, pred_ids, pred_n);
+}
+
 }  // namespace
 
 cudaError_t launch_stage(const Geom& G, const LayerState& S, const ReqTables& T, int32_t n_active,
@@ -424,25 +405,21 @@ cudaError_t launch_stage(const Geom& G, const LayerState& S, const ReqTables& T,
   if (n_active <= 0) return cudaSuccess;
   const int32_t nb_cap = max_nb > 0 ? max_nb : 1;
   const int32_t chunks = (nb_cap + kScoreChunk - 1) / kScoreChunk;
-  int32_t kp2 = 1;
-  while (kp2 < G.kb) kp2 <<= 1;
-  const size_t smem_select = (size_t)(kp2 + G.kb) * 8 + (size_t)(nb_cap + 256) * 4 + (size_t)6 * G.kb * 4 + 36 * 4;
-  const size_t smem_score = (size_t)2 * G.d * 4;
-  const size_t smem = smem_select > smem_score ? smem_select : smem_score;
+  const size_t need_score = 16 + coef_bytes(G);
+  const size_t need_select = 16 + select_bytes(G, nb_cap);
+  const size_t smem = need_score > need_select ? need_score : need_select;
   const int grid = n_active * G.Hkv * chunks;
   cudaError_t e;
   if (G.dtype == OKV_F32) {
     e = cudaFuncSetAttribute(stage_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    stage_kernel<float><<<grid, kScoreThreads, smem, s>>>(G, S, T, chunks, nb_cap, kp2, (const float*)draft,
-                                                          scores, arrivals, cap_blocks, step, ctr, err, pred_ids,
-                                                          pred_n);
+    stage_kernel<float><<<grid, kStageThreads, smem, s>>>(G, S, T, chunks, nb_cap, (const float*)draft, scores,
+                                                          arrivals, cap_blocks, step, ctr, err, pred_ids, pred_n);
   } else {
-    e = cudaFuncSetAttribute(stage_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
+    e = cudaFuncSetAttribute(stage_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    stage_kernel<__nv_bfloat16><<<grid, kScoreThreads, smem, s>>>(
-        G, S, T, chunks, nb_cap, kp2, (const __nv_bfloat16*)draft, scores, arrivals, cap_blocks, step, ctr, err,
+    stage_kernel<__nv_bfloat16><<<grid, kStageThreads, smem, s>>>(
+        G, S, T, chunks, nb_cap, (const __nv_bfloat16*)draft, scores, arrivals, cap_blocks, step, ctr, err,
         pred_ids, pred_n);
   }
   e = cudaGetLastError();

@@ -93,11 +93,13 @@ __global__ void append_kernel(Geom G, LayerState S, ReqTables T_, int32_t layer,
   T* host = reinterpret_cast<T*>(T_.host_kv[r] +
                                  (((int64_t)layer * G.Hkv + h) * cap + b) * G.block_bytes);
   const int64_t unit = (int64_t)r * G.Hkv + h;
-  const int32_t slot = S.resident[unit * G.nb_max + b];
-  if (slot >= G.kb) {
-    if (threadIdx.x == 0) record_error(err, kErrSlotRange, layer, r, slot);
-    return;
-  }
+  __shared__ int32_t tail_slot;  // slot holding the tail block, or -1
+  if (threadIdx.x == 0) tail_slot = -1;
+  __syncthreads();
+  for (int32_t s = threadIdx.x; s < G.kb; s += blockDim.x)
+    if (S.slot_block[unit * G.kb + s] == b) tail_slot = s;
+  __syncthreads();
+  const int32_t slot = tail_slot;
   T* pool = slot >= 0 ? reinterpret_cast<T*>(S.pool + (unit * G.kb + slot) * G.block_bytes) : nullptr;
   T* summ = reinterpret_cast<T*>(S.summ) + (unit * G.nb_max + b) * 2 * G.d;
   for (int32_t c = threadIdx.x; c < G.d; c += blockDim.x) {
@@ -120,14 +122,13 @@ __global__ void append_kernel(Geom G, LayerState S, ReqTables T_, int32_t layer,
 }
 
 // grid (layers, Hkv): empty pool and tables of request `req` on every layer.
-__global__ void reset_request_kernel(Geom G, int16_t* resident, int32_t* slot_block, int32_t* stamp,
-                                     int32_t* n_sel, int32_t* n_fetch, int32_t* len, int32_t req,
-                                     int32_t n_tok, uint64_t host_kv, int32_t cap,
-                                     uint64_t* host_kv_tab, int32_t* cap_tab) {
+__global__ void reset_request_kernel(Geom G, int32_t* slot_block, int32_t* stamp, int32_t* n_sel,
+                                     int32_t* n_fetch, int32_t* len, int32_t req, int32_t n_tok,
+                                     uint64_t host_kv, int32_t cap, uint64_t* host_kv_tab,
+                                     int32_t* cap_tab) {
   const int32_t layer = blockIdx.x, h = blockIdx.y;
   const int64_t units = (int64_t)G.R * G.Hkv;
   const int64_t u = (int64_t)layer * units + (int64_t)req * G.Hkv + h;
-  for (int32_t i = threadIdx.x; i < G.nb_max; i += blockDim.x) resident[u * G.nb_max + i] = -1;
   for (int32_t i = threadIdx.x; i < G.kb; i += blockDim.x) {
     slot_block[u * G.kb + i] = -1;
     stamp[u * G.kb + i] = -1;
@@ -187,13 +188,13 @@ cudaError_t launch_append(const Geom& G, const LayerState& S, const ReqTables& T
   return cudaGetLastError();
 }
 
-cudaError_t launch_reset_request(const Geom& G, int16_t* resident, int32_t* slot_block,
-                                 int32_t* stamp, int32_t* n_sel, int32_t* n_fetch, int32_t* len,
-                                 int32_t req, int32_t n_tok, uint64_t host_kv, int32_t cap,
-                                 uint64_t* host_kv_tab, int32_t* cap_tab, cudaStream_t s) {
+cudaError_t launch_reset_request(const Geom& G, int32_t* slot_block, int32_t* stamp, int32_t* n_sel,
+                                 int32_t* n_fetch, int32_t* len, int32_t req, int32_t n_tok,
+                                 uint64_t host_kv, int32_t cap, uint64_t* host_kv_tab, int32_t* cap_tab,
+                                 cudaStream_t s) {
   dim3 grid(G.L, G.Hkv);
-  reset_request_kernel<<<grid, 256, 0, s>>>(G, resident, slot_block, stamp, n_sel, n_fetch, len, req,
-                                            n_tok, host_kv, cap, host_kv_tab, cap_tab);
+  reset_request_kernel<<<grid, 256, 0, s>>>(G, slot_block, stamp, n_sel, n_fetch, len, req, n_tok, host_kv,
+                                            cap, host_kv_tab, cap_tab);
   return cudaGetLastError();
 }
 

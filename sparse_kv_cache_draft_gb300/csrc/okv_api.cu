@@ -41,7 +41,6 @@ struct okv_ctx {
   // device state, [layers] x per-layer block
   uint8_t* summ = nullptr;
   uint8_t* pool = nullptr;
-  int16_t* resident = nullptr;
   int32_t* slot_block = nullptr;
   int32_t* stamp = nullptr;
   int32_t* sel_ids = nullptr;
@@ -120,7 +119,6 @@ LayerState layer_state(const okv_ctx* c, int32_t layer) {
   LayerState S;
   S.summ = c->summ + layer * c->summ_layer_bytes;
   S.pool = c->pool + layer * c->pool_layer_bytes;
-  S.resident = c->resident + layer * U * G.nb_max;
   S.slot_block = c->slot_block + layer * U * G.kb;
   S.stamp = c->stamp + layer * U * G.kb;
   S.sel_ids = c->sel_ids + layer * U * G.kb;
@@ -274,7 +272,7 @@ void okv_destroy(okv_ctx* c) {
   if (c->ev_in) cudaEventDestroy(c->ev_in);
   if (c->sel_stream) cudaStreamDestroy(c->sel_stream);
   if (c->copy_stream) cudaStreamDestroy(c->copy_stream);
-  void* bufs[] = {c->summ, c->pool, c->resident, c->slot_block, c->stamp, c->sel_ids, c->sel_scores,
+  void* bufs[] = {c->summ, c->pool, c->slot_block, c->stamp, c->sel_ids, c->sel_scores,
                   c->n_sel, c->fetch, c->n_fetch, c->len, c->active_dev, c->host_kv_dev, c->cap_dev,
                   c->err_dev, c->ctr_dev, c->partials, c->draft_buf, c->scores, c->stage_arrivals, c->attend_arrivals};
   for (void* p : bufs)
@@ -300,7 +298,7 @@ okv_status okv_create(const okv_config* cfg, okv_ctx** out) {
   if (k.budget_tokens < k.block_size || k.budget_tokens % k.block_size) return bad("budget must be a multiple of block_size");
   if (k.budget_tokens / k.block_size > 1024) return bad("at most 1024 slots per unit");
   if (k.max_requests <= 0 || k.max_blocks_per_request <= 0) return bad("sizes");
-  if (k.max_blocks_per_request > 32767) return bad("max_blocks_per_request must fit the int16 resident map");
+  if (k.max_blocks_per_request > 32767) return bad("max_blocks_per_request must be at most 32767");
   if (!(k.fetch_cap > 0.f) || k.fetch_cap > 1.f) return bad("fetch_cap must be in (0, 1]");
   if (k.dtype != OKV_F32 && k.dtype != OKV_BF16) return bad("dtype");
   c->cfg = k;
@@ -336,7 +334,6 @@ okv_status okv_create(const okv_config* cfg, okv_ctx** out) {
   c->pool_layer_bytes = U * G.kb * G.block_bytes;
   const int64_t L = G.L;
   bool ok = alloc((void**)&c->summ, L * c->summ_layer_bytes) && alloc((void**)&c->pool, L * c->pool_layer_bytes) &&
-            alloc((void**)&c->resident, L * U * G.nb_max * sizeof(int16_t)) &&
             alloc((void**)&c->slot_block, L * U * G.kb * 4) && alloc((void**)&c->stamp, L * U * G.kb * 4) &&
             alloc((void**)&c->sel_ids, L * U * G.kb * 4) && alloc((void**)&c->sel_scores, L * U * G.kb * 4) &&
             alloc((void**)&c->n_sel, L * U * 4) && alloc((void**)&c->fetch, L * U * G.kb * 8) &&
@@ -364,7 +361,6 @@ okv_status okv_create(const okv_config* cfg, okv_ctx** out) {
   auto ck = [&](cudaError_t e) {
     if (e != cudaSuccess && st == OKV_OK) st = fail(c, OKV_ECUDA, "okv_create: %s", cudaGetErrorString(e));
   };
-  ck(cudaMemset(c->resident, 0xFF, L * U * G.nb_max * sizeof(int16_t)));
   ck(cudaMemset(c->slot_block, 0xFF, L * U * G.kb * 4));
   ck(cudaMemset(c->stamp, 0xFF, L * U * G.kb * 4));
   ck(cudaMemset(c->n_sel, 0, L * U * 4));
@@ -484,9 +480,8 @@ okv_status okv_add_request(okv_ctx* c, int32_t req, void* host_kv, int32_t capac
       break;
     }
   }
-  OKV_CUDA(c, okv::launch_reset_request(G, c->resident, c->slot_block, c->stamp, c->n_sel, c->n_fetch, c->len, req,
-                                        n_tokens, (uint64_t)(uintptr_t)dptr, capacity_blocks, c->host_kv_dev,
-                                        c->cap_dev, s));
+  OKV_CUDA(c, okv::launch_reset_request(G, c->slot_block, c->stamp, c->n_sel, c->n_fetch, c->len, req, n_tokens,
+                                        (uint64_t)(uintptr_t)dptr, capacity_blocks, c->host_kv_dev, c->cap_dev, s));
   c->launches += 1;
   if (twin >= 0) {
     const size_t bytes = (size_t)G.Hkv * G.nb_max * 2 * G.d * G.elem;

@@ -34,7 +34,6 @@ struct Geom {
 struct LayerState {
   uint8_t* summ;        // [R][Hkv][nb_max][2][d] storage
   uint8_t* pool;        // [R][Hkv][kb][2][bs][d] storage
-  int16_t* resident;    // [R][Hkv][nb_max] block -> slot or -1
   int32_t* slot_block;  // [R][Hkv][kb] slot -> block or -1
   int32_t* stamp;       // [R][Hkv][kb]
   int32_t* sel_ids;     // [R][Hkv][kb]
@@ -67,10 +66,10 @@ cudaError_t launch_summary_build(const Geom& G, int32_t layer_begin, int32_t lay
 cudaError_t launch_append(const Geom& G, const LayerState& S, const ReqTables& T, int32_t n_active,
                           int32_t layer, const void* k_new, const void* v_new, int32_t* err,
                           cudaStream_t s);
-cudaError_t launch_reset_request(const Geom& G, int16_t* resident, int32_t* slot_block,
-                                 int32_t* stamp, int32_t* n_sel, int32_t* n_fetch, int32_t* len,
-                                 int32_t req, int32_t n_tok, uint64_t host_kv, int32_t cap,
-                                 uint64_t* host_kv_tab, int32_t* cap_tab, cudaStream_t s);
+cudaError_t launch_reset_request(const Geom& G, int32_t* slot_block, int32_t* stamp, int32_t* n_sel,
+                                 int32_t* n_fetch, int32_t* len, int32_t req, int32_t n_tok,
+                                 uint64_t host_kv, int32_t cap, uint64_t* host_kv_tab, int32_t* cap_tab,
+                                 cudaStream_t s);
 cudaError_t launch_advance(const LayerState& S, const ReqTables& T, int32_t n_active, cudaStream_t s);
 // Staging of one layer for every active unit: block scores (into `scores`, a [R][Hkv][nb_max]
 // uint32 workspace) by chunks of blocks; the last chunk of each unit to finish (counted in
