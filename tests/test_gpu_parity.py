@@ -255,3 +255,29 @@ def test_capsweep_workload(cap):
         assert counts[:3].max() <= O.fetch_cap_blocks(cap, rig.kb)
     finally:
         rig.close()
+
+
+def test_sync_deadline_reports_timeout():
+    """okv_sync's deadline: staging queued behind a long (bounded) kernel on the caller's stream is
+    still pending after 50 ms, so the call returns OKV_ETIMEOUT instead of waiting; once the
+    kernel ends, the same context syncs and its state matches the oracle."""
+    import torch
+    from sparse_kv_cache_draft_gb300 import binding
+    w = synth.WORKLOADS["tiny"]
+    rig = Rig(w)
+    try:
+        draft = rig.batch_queries(0, -1, 1)
+        draft_dev = rig.device_rows(draft, (w.q_heads, w.head_dim))  # (a pageable copy would wait out the sleep)
+        torch.cuda.synchronize()
+        torch.cuda._sleep(1_000_000_000)  # about half a second of GPU clock on the caller's stream
+        rig.ctx.stage(0, draft_dev, 0, 1.0)
+        assert rig.ctx.sync(50) == binding.ETIMEOUT
+        torch.cuda.synchronize()
+        assert rig.ctx.sync(60_000) == binding.OK
+        rig._ensure_summaries(0)
+        rig.model.score_topk(0, draft)
+        gsel, _ = rig.check_selection(0)
+        rig.model.select(0, rig.kb, 0, sel_override=gsel)
+        rig.check_tables(0)
+    finally:
+        rig.close()
