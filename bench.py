@@ -11,7 +11,8 @@ attention of the step's query over the resident slot pool, then staging from the
 gather of the admitted blocks), the staging overlapped with the later layers' attention.
 `value` = batch * steps / device time of the timed steps (inputs resident in HBM);
 `e2e` = the same through the C ABI with the step's queries and drafts copied from pinned host
-memory and the step's attention outputs copied back, inside the timed region.
+memory and the step's attention outputs copied back, inside the timed region (the copies of
+the neighbouring steps overlap the compute, on their own streams).
 
 Full KV lives in page-locked host memory. The 288 GiB of the full batch do not fit the host,
 so requests alias `--alias` distinct host buffers (request r reads buffer r mod alias); every
@@ -195,6 +196,19 @@ def pinned_h2d_gbs(nbytes=1 << 30, reps=5) -> float:
     return nbytes / (best / 1e3) / 1e9
 
 
+class PlainBuffer:
+    """Ordinary (pageable) host memory with the .ptr / .free() of a HostBuffer."""
+
+    def __init__(self, nbytes: int):
+        import numpy as np
+        self.a = np.empty(nbytes + 256, dtype=np.uint8)
+        self.ptr = (self.a.ctypes.data + 255) // 256 * 256
+        self.nbytes = nbytes
+
+    def free(self):
+        self.a = None
+
+
 # ---- workload setup ----------------------------------------------------------------------------
 
 class Workload:
@@ -225,15 +239,20 @@ class Workload:
         return Config(w.layers, w.q_heads, w.kv_heads, w.head_dim, w.block_size, w.budget_tokens, w.batch,
                       self.nb, w.fetch_cap, BF16)
 
-    def host_kv(self):
-        from sparse_kv_cache_draft_gb300 import HostBuffer
+    def host_kv(self, pinned: bool = True):
+        """The aliased host KV buffers, filled by the generator. pinned=False gives plain host
+        memory (the CPU oracle needs nothing else)."""
         cfg = self.config()
         t0 = time.time()
-        bufs = [HostBuffer(cfg.host_bytes(self.nb)) for _ in range(self.alias)]
+        if pinned:
+            from sparse_kv_cache_draft_gb300 import HostBuffer
+            bufs = [HostBuffer(cfg.host_bytes(self.nb)) for _ in range(self.alias)]
+        else:
+            bufs = [PlainBuffer(cfg.host_bytes(self.nb)) for _ in range(self.alias)]
         t1 = time.time()
         for k, b in enumerate(bufs):
             self.synth.fill_kv(b.ptr, self.w, k, 0, self.n_tok, self.nb, n_threads=self.threads)
-        log(f"host KV: {self.alias} x {cfg.host_bytes(self.nb) / 2**30:.2f} GiB pinned in {t1 - t0:.1f}s, "
+        log(f"host KV: {self.alias} x {cfg.host_bytes(self.nb) / 2**30:.2f} GiB allocated in {t1 - t0:.1f}s, "
             f"generated in {time.time() - t1:.1f}s")
         return bufs
 
@@ -375,22 +394,52 @@ def run_okv(args, dist: Dist):
     dist.barrier()
     ms_max = dist.max(ms)
 
-    # e2e: the same steps through the C ABI from pinned host inputs, outputs copied back
-    out_host = HostBuffer(per_step * 2)
-    oh = as_bf16(out_host.numpy(np.uint16, qshape))
-    q_in = torch.empty(qshape, dtype=torch.bfloat16, device="cuda")
-    d_in = torch.empty(qshape, dtype=torch.bfloat16, device="cuda")
+    # e2e: the same steps through the C ABI from pinned host inputs, outputs copied back. The
+    # copies overlap the compute as a caller would run them: step i+1's queries and drafts are
+    # copied in on one stream and step i's outputs copied out on another while step i computes
+    # (double-buffered device tensors, events guarding every reuse).
+    out_host = HostBuffer(2 * per_step * 2)
+    oh = as_bf16(out_host.numpy(np.uint16, (2,) + qshape))
+    q_in = [torch.empty(qshape, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    d_in = [torch.empty(qshape, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    o_dev = [torch.empty(qshape, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_loaded = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_saved = [torch.cuda.Event() for _ in range(2)]
     qh_t, dh_t = as_bf16(qh), as_bf16(dh)
+
+    def load(i):
+        b, t = i % 2, W + i
+        if i >= 2:
+            s_in.wait_event(ev_done[b])  # step i-2 has finished reading this buffer
+        with torch.cuda.stream(s_in):
+            q_in[b].copy_(qh_t[t], non_blocking=True)
+            d_in[b].copy_(dh_t[t + 1], non_blocking=True)
+        ev_loaded[b].record(s_in)
+
     torch.cuda.synchronize()
     dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for i, t in enumerate(range(W, W + K)):
-        q_in.copy_(qh_t[t], non_blocking=True)
-        d_in.copy_(dh_t[t + 1], non_blocking=True)
-        ctx.step(q_in, d_in, out, W + K + i + 1)
-        oh.copy_(out, non_blocking=True)
+    s_in.wait_stream(stream)
+    s_out.wait_stream(stream)
+    load(0)
+    for i in range(K):
+        b = i % 2
+        if i + 1 < K:
+            load(i + 1)
+        stream.wait_event(ev_loaded[b])
+        if i >= 2:
+            stream.wait_event(ev_saved[b])  # step i-2's output has left this buffer
+        ctx.step(q_in[b], d_in[b], o_dev[b], W + K + i + 1)
+        ev_done[b].record(stream)
+        s_out.wait_event(ev_done[b])
+        with torch.cuda.stream(s_out):
+            oh[b].copy_(o_dev[b], non_blocking=True)
+        ev_saved[b].record(s_out)
     ctx.join(stream)
+    stream.wait_stream(s_out)
     e1.record(stream)
     e1.synchronize()
     e2e_ms = dist.max(e0.elapsed_time(e1))
@@ -456,7 +505,7 @@ def run_reference(args, dist: Dist):
     if dist.rank != 0:
         return None
     wl = Workload(args.alias, args.threads, args.batch, args.layers, args.workload)
-    bufs = wl.host_kv()
+    bufs = wl.host_kv(pinned=False)
     n_layers_used = min(4, wl.L)
     t = OracleTimer(wl, bufs, range(n_layers_used))
     for l in range(n_layers_used):
