@@ -57,6 +57,8 @@ class Unit(ctypes.Structure):
         ("slot_block", ctypes.c_void_p), ("stamp", ctypes.c_void_p), ("scores", ctypes.c_void_p),
         ("sel_ids", ctypes.c_void_p), ("sel_scores", ctypes.c_void_p), ("n_sel", ctypes.c_void_p),
         ("fetch", ctypes.c_void_p), ("n_fetch", ctypes.c_void_p), ("out", ctypes.c_void_p),
+        ("local_cap", ctypes.c_int32), ("local_of", ctypes.c_void_p), ("local_used", ctypes.c_void_p),
+        ("route", ctypes.c_void_p),
     ]
 
 
@@ -77,6 +79,8 @@ def _load(path: str):
     L.oracle_topk.restype = i32
     L.oracle_select_update.argtypes = [vp, vp, vp, i32, vp, i32, i32, i32, vp]
     L.oracle_select_update.restype = i32
+    L.oracle_local_route.argtypes = [vp, vp, i32, vp, i32, vp]
+    L.oracle_local_route.restype = i32
     L.oracle_attend.argtypes = [vp, i32, vp, i32, i32, i32, i32, vp, i32, vp]
     L.oracle_dense_attend.argtypes = [vp, i32, i32, i32, i32, vp, i32, vp]
     L.oracle_append.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp]
@@ -157,6 +161,19 @@ def select_update(resident: np.ndarray, slot_block: np.ndarray, stamp: np.ndarra
     return fetch[:n].copy()
 
 
+def local_route(local_of: np.ndarray, local_used: np.ndarray, local_cap: int, fetch,
+                L=None) -> tuple[np.ndarray, int]:
+    """Routes a fetch list ([n][2] (block, slot)) through a request's decode-side tier.
+
+    Updates local_of ([nb] int32) and local_used (int32 array of one element) in place; returns
+    (route [n] int32, number of entries read from the full copy)."""
+    fetch = np.ascontiguousarray(np.asarray(fetch, dtype=np.int32).reshape(-1, 2))
+    route = np.full(max(1, len(fetch)), -1, dtype=np.int32)
+    n = (L or lib()).oracle_local_route(_p(local_of), _p(local_used), local_cap, _p(fetch),
+                                        len(fetch), _p(route))
+    return route[:len(fetch)].copy(), int(n)
+
+
 def attend(host_unit: np.ndarray, slot_block: np.ndarray, n_tok: int, bs: int, d: int,
            q: np.ndarray, L=None) -> np.ndarray:
     q = np.ascontiguousarray(q, dtype=host_unit.dtype)
@@ -191,10 +208,15 @@ class OracleModel:
     Host KV is read through raw addresses: ``req_ptrs[r]`` is request r's buffer, laid out
     [layers][kv_heads][cap_blocks[r]][2][bs][d] in the storage type (the same bytes the GPU
     library reads). Summaries and the per-unit tables live in numpy arrays here.
+
+    ``local_cap[r]`` >= 0 marks request r as partially staged: its fetch lists are also routed
+    through a decode-side tier of that many entries per unit (``local_of``, ``local_used``,
+    ``route``); -1 (the default) marks a request that holds its full KV.
     """
 
     def __init__(self, *, layers, q_heads, kv_heads, head_dim, block_size, budget_tokens,
-                 dtype, req_ptrs, cap_blocks, n_tok, n_threads=None, layers_kept=None):
+                 dtype, req_ptrs, cap_blocks, n_tok, n_threads=None, layers_kept=None,
+                 local_cap=None):
         self.L, self.Hq, self.Hkv, self.d, self.bs = layers, q_heads, kv_heads, head_dim, block_size
         self.g = q_heads // kv_heads
         self.kb = budget_tokens // block_size
@@ -220,6 +242,11 @@ class OracleModel:
         self.fetch = {l: np.zeros(shp + (self.kb, 2), dtype=np.int32) for l in self.layers_kept}
         self.n_fetch = {l: np.zeros(shp, dtype=np.int32) for l in self.layers_kept}
         self.scores = {l: np.zeros(shp + (self.nb_max,), dtype=np.float32) for l in self.layers_kept}
+        self.local_cap = np.full(self.B, -1, dtype=np.int32) if local_cap is None else \
+            np.array(np.broadcast_to(np.asarray(local_cap, dtype=np.int32), (self.B,)))
+        self.local_of = {l: np.full(shp + (self.nb_max,), -1, dtype=np.int32) for l in self.layers_kept}
+        self.local_used = {l: np.zeros(shp, dtype=np.int32) for l in self.layers_kept}
+        self.route = {l: np.full(shp + (self.kb,), -1, dtype=np.int32) for l in self.layers_kept}
 
     def host_unit_ptr(self, layer: int, r: int, h: int) -> int:
         unit = int(self.cap_blocks[r]) * 2 * self.bs * self.d
@@ -263,6 +290,10 @@ class OracleModel:
                 u.n_fetch = self.n_fetch[layer][r, h:h + 1].ctypes.data
                 if out is not None:
                     u.out = out[r, h * self.g:(h + 1) * self.g].ctypes.data
+                u.local_cap = int(self.local_cap[r])
+                u.local_of = self.local_of[layer][r, h].ctypes.data
+                u.local_used = self.local_used[layer][r, h:h + 1].ctypes.data
+                u.route = self.route[layer][r, h].ctypes.data
                 units.append(u)
         return (Unit * len(units))(*units), keep
 

@@ -207,6 +207,38 @@ int32_t oracle_select_update(int32_t* resident, int32_t* slot_block, int32_t* st
   return n_admit;
 }
 
+/* ---- Decode-side tier of a request admitted with partial staging ("4 System Design", last
+ *      bullet: the full KV cache of a request stays in the prefill side's host memory until the
+ *      request completes, and the decode side keeps only the subset that decoding has asked for).
+ *      Reading: the fetch list is walked in order; a block the decode side already holds is read
+ *      from its kept copy; a block fetched for the first time is read from the full copy and kept
+ *      in the next unused entry of the decode-side tier; kept blocks stay until the request ends;
+ *      once the tier's `local_cap` entries are used, first-time blocks are read from the full copy
+ *      and not kept. route[i] = 2 * entry (read the kept copy), 2 * entry + 1 (read the full copy
+ *      and keep it in that entry), or -1 (read the full copy only). Returns the number of fetch
+ *      entries read from the full copy. --------------------------------------------------------- */
+
+int32_t oracle_local_route(int32_t* local_of, int32_t* local_used, int32_t local_cap,
+                           const int32_t* fetch, int32_t n_fetch, int32_t* route) {
+  int32_t from_full = 0;
+  for (int32_t i = 0; i < n_fetch; ++i) {
+    const int32_t b = fetch[2 * i + 0];
+    if (local_of[b] >= 0) {
+      route[i] = 2 * local_of[b];
+      continue;
+    }
+    ++from_full;
+    if (*local_used < local_cap) {
+      local_of[b] = *local_used;
+      *local_used += 1;
+      route[i] = 2 * local_of[b] + 1;
+    } else {
+      route[i] = -1;
+    }
+  }
+  return from_full;
+}
+
 /* ---- S6: attention over the resident set ("4 System Design": attention runs over the
  *      resident KV). Reading: every valid token of every occupied slot; scale 1/sqrt(d);
  *      keys already carry their positions; an empty set yields zeros. ----------------------- */
@@ -315,6 +347,12 @@ static void run_unit(oracle_unit* u, const oracle_dims* D, int32_t what) {
     const int32_t n = u->n_sel_override >= 0 ? u->n_sel_override : *u->n_sel;
     *u->n_fetch = oracle_select_update(u->resident, u->slot_block, u->stamp, D->kb, sel, n,
                                        D->cap_blocks, D->step, u->fetch);
+    if (u->route) {
+      if (u->local_cap >= 0)
+        oracle_local_route(u->local_of, u->local_used, u->local_cap, u->fetch, *u->n_fetch, u->route);
+      else
+        for (int32_t i = 0; i < *u->n_fetch; ++i) u->route[i] = -1;
+    }
   }
   if (what & ORACLE_DO_ATTEND)
     oracle_attend(u->host_unit, D->dtype, u->slot_block, D->kb, u->n_tok, D->bs, D->d, u->q, D->g,

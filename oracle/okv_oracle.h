@@ -13,7 +13,8 @@
  * Pins (tests/test_oracle_*.py): closed-form KV sizing from "2 Background";
  * brute-force min/max; the score's upper-bound property and its one-token special
  * case; brute-force sorting for top-K; the selection rules of "4 System Design"
- * checked as invariants plus hand-worked scenarios; sparse attention equal to a
+ * checked as invariants plus hand-worked scenarios; the decode-side tier against a
+ * first-demand set computation and a hand-worked scenario; sparse attention equal to a
  * textbook dense softmax attention when the budget covers the context; one-token
  * and equal-score special cases; appends equal to a rebuild.
  */
@@ -54,6 +55,14 @@ int32_t oracle_topk(const float* scores, int32_t nb, int32_t kb, int32_t* ids);
 int32_t oracle_select_update(int32_t* resident, int32_t* slot_block, int32_t* stamp, int32_t kb,
                              const int32_t* sel, int32_t n_sel, int32_t cap_blocks, int32_t step,
                              int32_t* fetch);
+
+/* Decode-side tier of a partially staged request (see the .c file): walks the fetch list
+ * ([n_fetch][2] (block, slot)) in order and writes route[i] = 2*entry (read the kept copy),
+ * 2*entry + 1 (read the full copy, keep it in that entry) or -1 (read the full copy only);
+ * local_of: [nb] block -> kept entry or -1; *local_used: entries in use (at most local_cap).
+ * Returns how many entries read the full copy. */
+int32_t oracle_local_route(int32_t* local_of, int32_t* local_used, int32_t local_cap,
+                           const int32_t* fetch, int32_t n_fetch, int32_t* route);
 
 /* Softmax attention of g query heads over every valid token of every block named in
  * slot_block (entries >= 0), reading K and V from host_unit. out: [g][d]. */
@@ -96,6 +105,10 @@ typedef struct {
   int32_t* fetch;           /* [kb][2] */
   int32_t* n_fetch;
   double* out;              /* [g][d] */
+  int32_t local_cap;        /* < 0: the request holds its full KV; else decode-side tier entries */
+  int32_t* local_of;        /* [nb] block -> decode-side entry or -1 (local_cap >= 0) */
+  int32_t* local_used;      /* entries in use (local_cap >= 0) */
+  int32_t* route;           /* [kb] or NULL: SELECT also routes its fetch list (-1 for full KV) */
 } oracle_unit;
 
 typedef struct {

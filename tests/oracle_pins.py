@@ -271,6 +271,62 @@ def pin_select_invariants(L):
             assert set(int(b) for b in slot_block if b >= 0) == set(range(nb))
 
 
+# ---- decode-side tier (partial staging) -------------------------------------------------------
+
+def pin_local_tier_golden(L):
+    for sc in _golden("local_tier_scenarios.json")["scenarios"]:
+        local_of = np.full(sc["nb"], -1, np.int32)
+        used = np.zeros(1, np.int32)
+        for st in sc["steps"]:
+            fetch = [[b, i] for i, b in enumerate(st["fetch"])]
+            route, n_full = oracle.local_route(local_of, used, sc["local_cap"], fetch, L)
+            assert route.tolist() == st["route"], (sc["name"], route.tolist())
+            assert int(used[0]) == st["local_used"] and n_full == st["from_full"], (sc["name"], used, n_full)
+            kept = {str(b): int(e) for b, e in enumerate(local_of) if e >= 0}
+            assert kept == st["kept"], (sc["name"], kept)
+
+
+def pin_local_tier_first_demand(L):
+    # Fetch lists from real selection runs; the decode-side tier must hold exactly the first
+    # local_cap distinct blocks in order of first demand, numbered in that order, and every other
+    # fetch must read the full copy.
+    rng = np.random.default_rng(23)
+    for trial in range(30):
+        nb = int(rng.integers(4, 80))
+        kb = int(rng.integers(2, 20))
+        C = int(rng.integers(1, kb + 1))
+        local_cap = int(rng.choice([0, 1, int(rng.integers(1, nb + 1)), nb]))
+        resident = np.full(nb, -1, np.int32)
+        slot_block = np.full(kb, -1, np.int32)
+        stamp = np.full(kb, -1, np.int32)
+        local_of = np.full(nb, -1, np.int32)
+        used = np.zeros(1, np.int32)
+        demanded = []  # every fetched block, in order
+        for step in range(15):
+            sel = rng.permutation(nb)[:min(kb, nb)].astype(np.int32)
+            fetch = oracle.select_update(resident, slot_block, stamp, sel, C, step, L)
+            route, n_full = oracle.local_route(local_of, used, local_cap, fetch, L)
+            first_order = list(dict.fromkeys(demanded + [int(b) for b in fetch[:, 0]]))
+            kept = first_order[:local_cap]
+            entry = {b: e for e, b in enumerate(kept)}
+            want, full = [], 0
+            for b in (int(x) for x in fetch[:, 0]):
+                if b in entry and b in demanded:
+                    want.append(2 * entry[b])
+                elif b in entry:
+                    want.append(2 * entry[b] + 1)
+                    full += 1
+                else:
+                    want.append(-1)
+                    full += 1
+                demanded.append(b)
+            assert route.tolist() == want, (trial, step, route.tolist(), want)
+            assert n_full == full and int(used[0]) == len(kept) <= local_cap
+            assert {b: int(e) for b, e in enumerate(local_of) if e >= 0} == entry
+        if local_cap >= nb:  # ample entries: each block crosses from the full copy once
+            assert int(used[0]) == len(set(demanded))
+
+
 # ---- attention --------------------------------------------------------------------------------
 
 def pin_attend_dense_textbook(L):

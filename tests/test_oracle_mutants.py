@@ -40,6 +40,10 @@ MUTANTS = {
     "select_ignores_stamp": ("if (x->stamp != y->stamp) return (x->stamp > y->stamp) - (x->stamp < y->stamp);", ""),
     "select_no_stamp_on_hit": ("      stamp[s] = step;\n      hit_slot[s] = 1;", "      hit_slot[s] = 1;"),
     "select_evicted_stays_mapped": ("if (old >= 0) resident[old] = -1;", ""),
+    "local_ignores_capacity": ("if (*local_used < local_cap) {", "if (1) {"),
+    "local_fill_marked_as_hit": ("route[i] = 2 * local_of[b] + 1;", "route[i] = 2 * local_of[b];"),
+    "local_entry_off_by_one": ("local_of[b] = *local_used;", "local_of[b] = *local_used + 1;"),
+    "local_full_reads_uncounted": ("    ++from_full;\n    if (*local_used", "    if (*local_used"),
     "attend_no_scale": ("z[k] = dot * scale;", "z[k] = dot;"),
     "attend_values_from_keys": ("z[k] * load(host_unit, dtype, v_off(b, t, c, bs, d));",
                                 "z[k] * load(host_unit, dtype, k_off(b, t, c, bs, d));"),
