@@ -93,6 +93,28 @@ OKV_API okv_status okv_host_free(void* p);
  * ESTATE if req is already active. */
 OKV_API okv_status okv_add_request(okv_ctx* ctx, int32_t req, void* host_kv, int32_t capacity_blocks,
                            int32_t n_tokens, void* stream);
+/* Register request `req` with admission-time partial staging ("4 System Design", last bullet:
+ * the prefill side keeps each request's full KV cache in its host memory until the request
+ * completes, and the decode side materialises only a demand-filled subset of it).
+ *   full_kv:  the full copy, page-locked, host KV layout with capacity_blocks blocks per unit.
+ *             It stands for the prefill side's memory; the caller keeps it alive until
+ *             okv_remove_request.
+ *   local_kv: the decode-side tier, page-locked, host KV layout with local_capacity_blocks
+ *             entries per unit, [layers][kv_heads][local_capacity_blocks][2][block_size]
+ *             [head_dim]; caller-owned, written by the library; NULL if local_capacity_blocks
+ *             is 0. It may not overlap any active request's buffers.
+ * Summaries are built from full_kv as in okv_add_request (the prefill side's work). Then every
+ * fetch of a block by okv_stage reads the decode side's kept copy if it has one; a block fetched
+ * for the first time is read from full_kv and kept in the next unused entry of its unit (entries
+ * are taken in fetch order and never released before okv_remove_request); once a unit's entries
+ * are used up, first-time blocks are read from full_kv without being kept. okv_append writes
+ * full_kv and, if the block is kept, the kept copy. The okv_timing counters local_hits,
+ * local_fills and full_reads count these fetches; okv_read_local returns the tables.
+ * EINVAL: as okv_add_request, or local_capacity_blocks outside [0, capacity_blocks], or local_kv
+ * unpinned, unaligned or overlapping; ESTATE if req is already active. */
+OKV_API okv_status okv_add_request_partial(okv_ctx* ctx, int32_t req, void* full_kv, int32_t capacity_blocks,
+                                           void* local_kv, int32_t local_capacity_blocks, int32_t n_tokens,
+                                           void* stream);
 /* Forget request `req` (its pool slots become free). Synchronises the internal streams. */
 OKV_API okv_status okv_remove_request(okv_ctx* ctx, int32_t req);
 
@@ -182,6 +204,14 @@ OKV_API okv_status okv_read_fetch_list(okv_ctx* ctx, int32_t layer, int32_t* cou
 OKV_API okv_status okv_read_pool(okv_ctx* ctx, int32_t layer, int32_t req, int32_t kv_head, void* out);
 /* Current context length of every request at a layer: lengths [max_requests] (0 if inactive). */
 OKV_API okv_status okv_read_lengths(okv_ctx* ctx, int32_t layer, int32_t* lengths);
+/* Decode-side tiers of partially staged requests at a layer: local_used [max_requests][kv_heads]
+ * (entries in use); local_of [max_requests][kv_heads][max_blocks_per_request] (kept entry of each
+ * block or -1); routes [max_requests][kv_heads][Kb], one per entry of the last fetch list:
+ * 2*e = read from kept entry e, 2*e + 1 = read from the full copy and kept in entry e, -1 = read
+ * from the full copy only (always -1 for requests registered with okv_add_request). Rows of
+ * other requests hold no meaning. Any array may be NULL. */
+OKV_API okv_status okv_read_local(okv_ctx* ctx, int32_t layer, int32_t* local_used, int32_t* local_of,
+                                  int32_t* routes);
 
 /* ---- measurement ---- */
 
@@ -195,6 +225,10 @@ typedef struct {
   int64_t launches[OKV_K_COUNT];  /* kernel launches of each kind */
   int64_t fetched_blocks;         /* blocks gathered host -> HBM */
   int64_t attended_slots;         /* occupied slots read by attention launches */
+  /* fetches of partially staged requests (okv_add_request_partial): */
+  int64_t local_hits;             /* read from the decode side's kept copy */
+  int64_t local_fills;            /* read from the full copy and kept */
+  int64_t full_reads;             /* read from the full copy (local_fills included) */
 } okv_timing;
 
 /* Enable (1) or disable (0) per-launch CUDA-event timing; resets the totals. */

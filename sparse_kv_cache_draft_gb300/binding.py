@@ -43,7 +43,8 @@ class _Config(ctypes.Structure):
 
 class _Timing(ctypes.Structure):
     _fields_ = [("ms", ctypes.c_double * 7), ("launches", ctypes.c_int64 * 7),
-                ("fetched_blocks", ctypes.c_int64), ("attended_slots", ctypes.c_int64)]
+                ("fetched_blocks", ctypes.c_int64), ("attended_slots", ctypes.c_int64),
+                ("local_hits", ctypes.c_int64), ("local_fills", ctypes.c_int64), ("full_reads", ctypes.c_int64)]
 
 
 def load_library():
@@ -67,6 +68,7 @@ def load_library():
             "okv_host_alloc": ([i64, ctypes.POINTER(vp)], st),
             "okv_host_free": ([vp], st),
             "okv_add_request": ([vp, i32, vp, i32, i32, vp], st),
+            "okv_add_request_partial": ([vp, i32, vp, i32, vp, i32, i32, vp], st),
             "okv_remove_request": ([vp, i32], st),
             "okv_append": ([vp, i32, vp, vp, vp], st),
             "okv_stage": ([vp, i32, vp, i32, f32, vp], st),
@@ -82,6 +84,7 @@ def load_library():
             "okv_read_fetch_list": ([vp, i32, vp, vp], st),
             "okv_read_pool": ([vp, i32, i32, i32, vp], st),
             "okv_read_lengths": ([vp, i32, vp], st),
+            "okv_read_local": ([vp, i32, vp, vp, vp], st),
             "okv_set_timing": ([vp, i32], st),
             "okv_read_timing": ([vp, ctypes.POINTER(_Timing)], st),
             "okv_launch_count": ([vp], i64),
@@ -216,6 +219,13 @@ class Context:
         self._check(self.L.okv_add_request(self.h, req, ctypes.c_void_p(host_ptr), capacity_blocks, n_tokens,
                                            ctypes.c_void_p(_stream_handle(stream))), "okv_add_request")
 
+    def add_request_partial(self, req: int, full_ptr: int, capacity_blocks: int, local_ptr: int,
+                            local_capacity_blocks: int, n_tokens: int, stream=None):
+        self._check(self.L.okv_add_request_partial(self.h, req, ctypes.c_void_p(full_ptr), capacity_blocks,
+                                                   ctypes.c_void_p(local_ptr or None), local_capacity_blocks,
+                                                   n_tokens, ctypes.c_void_p(_stream_handle(stream))),
+                    "okv_add_request_partial")
+
     def remove_request(self, req: int):
         self._check(self.L.okv_remove_request(self.h, req), "okv_remove_request")
 
@@ -314,6 +324,16 @@ class Context:
         self._check(self.L.okv_read_lengths(self.h, layer, _np_ptr(out)), "okv_read_lengths")
         return out
 
+    def read_local(self, layer: int):
+        """(local_used [R][Hkv], local_of [R][Hkv][max_blocks], routes [R][Hkv][Kb])."""
+        c = self.cfg
+        used = np.empty((c.max_requests, c.kv_heads), np.int32)
+        local_of = np.empty((c.max_requests, c.kv_heads, c.max_blocks_per_request), np.int32)
+        routes = np.empty((c.max_requests, c.kv_heads, c.slots), np.int32)
+        self._check(self.L.okv_read_local(self.h, layer, _np_ptr(used), _np_ptr(local_of), _np_ptr(routes)),
+                    "okv_read_local")
+        return used, local_of, routes
+
     def set_timing(self, enable: bool):
         self._check(self.L.okv_set_timing(self.h, 1 if enable else 0), "okv_set_timing")
 
@@ -322,7 +342,9 @@ class Context:
         self._check(self.L.okv_read_timing(self.h, ctypes.byref(t)), "okv_read_timing")
         return {"ms": {k: t.ms[i] for i, k in enumerate(KERNEL_KINDS)},
                 "launches": {k: int(t.launches[i]) for i, k in enumerate(KERNEL_KINDS)},
-                "fetched_blocks": int(t.fetched_blocks), "attended_slots": int(t.attended_slots)}
+                "fetched_blocks": int(t.fetched_blocks), "attended_slots": int(t.attended_slots),
+                "local_hits": int(t.local_hits), "local_fills": int(t.local_fills),
+                "full_reads": int(t.full_reads)}
 
     def launch_count(self) -> int:
         return int(self.L.okv_launch_count(self.h))

@@ -5,6 +5,11 @@
 // forward pass. Here the SMs read the host buffer directly over the host link (the buffer is
 // device-mapped), one warp per block: every lane issues all of its 16-byte loads of the block
 // before storing, so a warp keeps a whole block in flight.
+//
+// Partially staged requests (same section, last bullet: the prefill side keeps the full KV
+// cache until the request completes, the decode side a demand-filled subset): a block comes
+// from the decode side's kept copy when it has one; a block fetched for the first time comes
+// from the full copy and is also written to the decode-side entry the selection assigned.
 #include <stdlib.h>
 
 #include "okv_internal.h"
@@ -49,6 +54,26 @@ gather_kernel(Geom G, LayerState S, ReqTables RT, int32_t layer, int32_t n_units
     const uint4* src = reinterpret_cast<const uint4*>(
         RT.host_kv[r] + (((int64_t)layer * G.Hkv + h) * cap + b) * G.block_bytes);
     uint4* dst = reinterpret_cast<uint4*>(S.pool + (unit * G.kb + s) * G.block_bytes);
+    uint4* keep = nullptr;  // decode-side copy to fill, if any
+    const int32_t lcap = RT.local_cap[r];
+    if (lcap >= 0) {
+      // partially staged request: read the decode side's kept copy, or read the full copy and
+      // keep it in the entry the selection assigned
+      const int32_t route = S.route[unit * G.kb + e];
+      if (route >= 0) {
+        const int32_t ent = route >> 1;
+        if (ent >= lcap) {
+          if (lane == 0) record_error(err, kErrLocalRange, layer, r, ent);
+          continue;
+        }
+        uint4* kept = reinterpret_cast<uint4*>(RT.local_kv[r] +
+                                               (((int64_t)layer * G.Hkv + h) * lcap + ent) * G.block_bytes);
+        if (route & 1)
+          keep = kept;
+        else
+          src = kept;
+      }
+    }
     for (int32_t base = 0; base < nvec; base += 32 * kVecPerLane) {
       uint4 x[kVecPerLane];
 #pragma unroll
@@ -60,6 +85,13 @@ gather_kernel(Geom G, LayerState S, ReqTables RT, int32_t layer, int32_t n_units
       for (int i = 0; i < kVecPerLane; ++i) {
         const int32_t v = base + i * 32 + lane;
         if (v < nvec) __stcs(dst + v, x[i]);
+      }
+      if (keep) {
+#pragma unroll
+        for (int i = 0; i < kVecPerLane; ++i) {
+          const int32_t v = base + i * 32 + lane;
+          if (v < nvec) __stcs(keep + v, x[i]);
+        }
       }
     }
   }

@@ -169,9 +169,12 @@ __host__ __device__ inline size_t select_bytes(const Geom& G, int32_t nb_cap) {
          (size_t)6 * G.kb * 4 + 40 * 4;
 }
 
+// lcap >= 0: the request is partially staged with a decode-side tier of lcap entries per unit,
+// and its fetch list is routed through that tier (S.route).
 __device__ void select_unit(const Geom& G, const LayerState& S, int32_t r, int32_t h, int32_t nb,
                             int32_t nb_cap, const uint32_t* ord_in, int32_t cap_blocks, int32_t step,
-                            Counters* ctr, int32_t* err, uint8_t* smem, int32_t* pred_ids, int32_t* pred_n) {
+                            int32_t lcap, Counters* ctr, int32_t* err, uint8_t* smem, int32_t* pred_ids,
+                            int32_t* pred_n) {
   const size_t kp = pow2_at_least((size_t)nb_cap > (size_t)G.kb ? (size_t)nb_cap : (size_t)G.kb);
   unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem);  // [kp] candidates
   unsigned long long* tkey = keys + kp;                                    // [kb] eviction order
@@ -184,6 +187,7 @@ __device__ void select_unit(const Geom& G, const LayerState& S, int32_t r, int32
   int32_t* target = hit + G.kb;   // [kb]
   int32_t* selid = target + G.kb; // [kb] selection, in order
   int32_t* missrank = selid + G.kb;  // [kb] rank of a miss, or -1
+  int32_t* fblk = hit;            // [kb] block of each fetch entry (reuses `hit` once it is read)
   int32_t* scratch = missrank + G.kb;  // [40]
 
   const int64_t unit = (int64_t)r * G.Hkv + h;
@@ -349,10 +353,39 @@ __device__ void select_unit(const Geom& G, const LayerState& S, int32_t r, int32
     const int32_t s = target[rk];
     sb[s] = b;
     st[s] = step;
+    fblk[rk] = b;
     S.fetch[(unit * G.kb + rk) * 2 + 0] = b;
     S.fetch[(unit * G.kb + rk) * 2 + 1] = s;
   }
   __syncthreads();
+
+  // ---- decode-side tier (partially staged requests): in fetch order, a block already kept is
+  // read from its entry; the k-th block fetched for the first time is read from the full copy
+  // and kept in entry used + k while entries remain, else read from the full copy only ----
+  int32_t n_fresh = 0;
+  const int32_t used0 = lcap >= 0 ? S.local_used[unit] : 0;
+  if (lcap < 0) {
+    for (int32_t i = tid; i < n_admit; i += blockDim.x) S.route[unit * G.kb + i] = -1;
+  } else {
+    for (int32_t i0 = 0; i0 < n_admit; i0 += blockDim.x) {
+      const int32_t i = i0 + tid;
+      const int32_t e = i < n_admit ? S.local_of[unit * G.nb_max + fblk[i]] : 0;
+      const bool fresh = i < n_admit && e < 0;
+      int32_t n;
+      const int32_t k = n_fresh + block_rank(fresh, scratch, &n);
+      n_fresh += n;
+      if (i >= n_admit) continue;
+      int32_t route = 2 * e;
+      if (fresh) {
+        route = -1;
+        if (used0 + k < lcap) {
+          route = 2 * (used0 + k) + 1;
+          S.local_of[unit * G.nb_max + fblk[i]] = used0 + k;
+        }
+      }
+      S.route[unit * G.kb + i] = route;
+    }
+  }
   for (int32_t s = tid; s < G.kb; s += blockDim.x) {
     S.slot_block[unit * G.kb + s] = sb[s];
     S.stamp[unit * G.kb + s] = st[s];
@@ -360,6 +393,14 @@ __device__ void select_unit(const Geom& G, const LayerState& S, int32_t r, int32
   if (tid == 0) {
     S.n_fetch[unit] = n_admit;
     if (n_admit > 0) atomicAdd(&ctr->fetched_blocks, (unsigned long long)n_admit);
+    if (lcap >= 0 && n_admit > 0) {
+      const int32_t room = lcap - used0 > 0 ? lcap - used0 : 0;
+      const int32_t fills = n_fresh < room ? n_fresh : room;
+      S.local_used[unit] = used0 + fills;
+      atomicAdd(&ctr->local_hits, (unsigned long long)(n_admit - n_fresh));
+      atomicAdd(&ctr->local_fills, (unsigned long long)fills);
+      atomicAdd(&ctr->full_reads, (unsigned long long)n_fresh);
+    }
   }
 }
 
@@ -392,7 +433,8 @@ stage_kernel(Geom G, LayerState S, ReqTables RT, int32_t chunks, int32_t nb_cap,
   __syncthreads();
   if (!last || bad) return;
   __threadfence();
-  select_unit(G, S, r, h, nb, nb_cap, ord, cap_blocks, step, ctr, err, smem + 16, pred_ids, pred_n);
+  select_unit(G, S, r, h, nb, nb_cap, ord, cap_blocks, step, RT.local_cap[r], ctr, err, smem + 16, pred_ids,
+              pred_n);
 }
 
 }  // namespace

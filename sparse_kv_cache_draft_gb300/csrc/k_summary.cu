@@ -101,6 +101,18 @@ __global__ void append_kernel(Geom G, LayerState S, ReqTables T_, int32_t layer,
   __syncthreads();
   const int32_t slot = tail_slot;
   T* pool = slot >= 0 ? reinterpret_cast<T*>(S.pool + (unit * G.kb + slot) * G.block_bytes) : nullptr;
+  // a partially staged request also writes the decode side's kept copy of the block, if any
+  T* kept = nullptr;
+  const int32_t lcap = T_.local_cap[r];
+  if (lcap > 0) {
+    const int32_t e = S.local_of[unit * G.nb_max + b];
+    if (e >= lcap) {
+      if (threadIdx.x == 0) record_error(err, kErrLocalRange, layer, r, e);
+      return;
+    }
+    if (e >= 0)
+      kept = reinterpret_cast<T*>(T_.local_kv[r] + (((int64_t)layer * G.Hkv + h) * lcap + e) * G.block_bytes);
+  }
   T* summ = reinterpret_cast<T*>(S.summ) + (unit * G.nb_max + b) * 2 * G.d;
   for (int32_t c = threadIdx.x; c < G.d; c += blockDim.x) {
     const T k = k_new[unit * G.d + c];
@@ -110,6 +122,10 @@ __global__ void append_kernel(Geom G, LayerState S, ReqTables T_, int32_t layer,
     if (pool) {
       pool[kofs + c] = k;
       pool[vofs + c] = v;
+    }
+    if (kept) {
+      kept[kofs + c] = k;
+      kept[vofs + c] = v;
     }
     if (t == 0) {
       summ[c] = k;
@@ -121,25 +137,26 @@ __global__ void append_kernel(Geom G, LayerState S, ReqTables T_, int32_t layer,
   }
 }
 
-// grid (layers, Hkv): empty pool and tables of request `req` on every layer.
-__global__ void reset_request_kernel(Geom G, int32_t* slot_block, int32_t* stamp, int32_t* n_sel,
-                                     int32_t* n_fetch, int32_t* len, int32_t req, int32_t n_tok,
-                                     uint64_t host_kv, int32_t cap, uint64_t* host_kv_tab,
-                                     int32_t* cap_tab) {
+// grid (layers, Hkv): empty pool, tables and decode-side tier of one request on every layer.
+__global__ void reset_request_kernel(Geom G, StateBase B, RequestInit q) {
   const int32_t layer = blockIdx.x, h = blockIdx.y;
   const int64_t units = (int64_t)G.R * G.Hkv;
-  const int64_t u = (int64_t)layer * units + (int64_t)req * G.Hkv + h;
+  const int64_t u = (int64_t)layer * units + (int64_t)q.req * G.Hkv + h;
   for (int32_t i = threadIdx.x; i < G.kb; i += blockDim.x) {
-    slot_block[u * G.kb + i] = -1;
-    stamp[u * G.kb + i] = -1;
+    B.slot_block[u * G.kb + i] = -1;
+    B.stamp[u * G.kb + i] = -1;
   }
+  for (int32_t i = threadIdx.x; i < G.nb_max; i += blockDim.x) B.local_of[u * G.nb_max + i] = -1;
   if (threadIdx.x == 0) {
-    n_sel[u] = 0;
-    n_fetch[u] = 0;
-    if (h == 0) len[(int64_t)layer * G.R + req] = n_tok;
+    B.n_sel[u] = 0;
+    B.n_fetch[u] = 0;
+    B.local_used[u] = 0;
+    if (h == 0) B.len[(int64_t)layer * G.R + q.req] = q.n_tok;
     if (h == 0 && layer == 0) {
-      host_kv_tab[req] = host_kv;
-      cap_tab[req] = cap;
+      B.host_kv_tab[q.req] = q.host_kv;
+      B.cap_tab[q.req] = q.cap;
+      B.local_kv_tab[q.req] = q.local_kv;
+      B.local_cap_tab[q.req] = q.local_cap;
     }
   }
 }
@@ -188,13 +205,9 @@ cudaError_t launch_append(const Geom& G, const LayerState& S, const ReqTables& T
   return cudaGetLastError();
 }
 
-cudaError_t launch_reset_request(const Geom& G, int32_t* slot_block, int32_t* stamp, int32_t* n_sel,
-                                 int32_t* n_fetch, int32_t* len, int32_t req, int32_t n_tok,
-                                 uint64_t host_kv, int32_t cap, uint64_t* host_kv_tab, int32_t* cap_tab,
-                                 cudaStream_t s) {
+cudaError_t launch_reset_request(const Geom& G, const StateBase& B, const RequestInit& q, cudaStream_t s) {
   dim3 grid(G.L, G.Hkv);
-  reset_request_kernel<<<grid, 256, 0, s>>>(G, slot_block, stamp, n_sel, n_fetch, len, req, n_tok, host_kv,
-                                            cap, host_kv_tab, cap_tab);
+  reset_request_kernel<<<grid, 256, 0, s>>>(G, B, q);
   return cudaGetLastError();
 }
 

@@ -52,6 +52,11 @@ struct okv_ctx {
   int32_t* active_dev = nullptr;
   uint64_t* host_kv_dev = nullptr;
   int32_t* cap_dev = nullptr;
+  int32_t* local_of = nullptr;     // [layers][R][Hkv][nb_max]
+  int32_t* local_used = nullptr;   // [layers][R][Hkv]
+  int32_t* route = nullptr;        // [layers][R][Hkv][kb]
+  uint64_t* local_kv_dev = nullptr;  // [R]
+  int32_t* local_cap_dev = nullptr;  // [R], -1 for a request that holds its full KV
   int32_t* err_dev = nullptr;
   Counters* ctr_dev = nullptr;
   void* partials = nullptr;
@@ -69,6 +74,8 @@ struct okv_ctx {
   std::vector<int32_t> active_list;    // compact
   std::vector<void*> host_ptr;         // [R]
   std::vector<int32_t> cap_blocks;     // [R]
+  std::vector<void*> local_ptr;        // [R] decode-side tier of a partially staged request
+  std::vector<int32_t> local_cap;      // [R] its entries per unit (-1: full-KV request)
   std::vector<int32_t> len_host;       // [L][R]
   std::vector<int> shared_buf;         // [R] host buffer shared with another active request
 
@@ -127,6 +134,9 @@ LayerState layer_state(const okv_ctx* c, int32_t layer) {
   S.fetch = c->fetch + layer * U * G.kb * 2;
   S.n_fetch = c->n_fetch + layer * U;
   S.len = c->len + (int64_t)layer * G.R;
+  S.local_of = c->local_of + layer * U * G.nb_max;
+  S.local_used = c->local_used + layer * U;
+  S.route = c->route + layer * U * G.kb;
   return S;
 }
 
@@ -135,6 +145,8 @@ ReqTables req_tables(const okv_ctx* c) {
   T.active = c->active_dev;
   T.host_kv = c->host_kv_dev;
   T.cap_blocks = c->cap_dev;
+  T.local_kv = c->local_kv_dev;
+  T.local_cap = c->local_cap_dev;
   return T;
 }
 
@@ -184,8 +196,8 @@ okv_status check_device_error(okv_ctx* c) {
     cudaMemcpy(c->err_dev, zero, sizeof(zero), cudaMemcpyHostToDevice);
     static const char* names[] = {"none", "block id out of range", "slot out of range",
                                   "append past capacity", "context length out of range",
-                                  "asynchronous copy wait timed out"};
-    const char* n = (e[0] >= 0 && e[0] <= 5) ? names[e[0]] : "unknown";
+                                  "asynchronous copy wait timed out", "decode-side entry out of range"};
+    const char* n = (e[0] >= 0 && e[0] <= 6) ? names[e[0]] : "unknown";
     return fail(c, OKV_EDEVICE, "device error %d (%s): layer/site %d, request %d, value %d", e[0], n,
                 e[1], e[2], e[3]);
   }
@@ -274,7 +286,8 @@ void okv_destroy(okv_ctx* c) {
   if (c->copy_stream) cudaStreamDestroy(c->copy_stream);
   void* bufs[] = {c->summ, c->pool, c->slot_block, c->stamp, c->sel_ids, c->sel_scores,
                   c->n_sel, c->fetch, c->n_fetch, c->len, c->active_dev, c->host_kv_dev, c->cap_dev,
-                  c->err_dev, c->ctr_dev, c->partials, c->draft_buf, c->scores, c->stage_arrivals, c->attend_arrivals};
+                  c->err_dev, c->ctr_dev, c->partials, c->draft_buf, c->scores, c->stage_arrivals, c->attend_arrivals,
+                  c->local_of, c->local_used, c->route, c->local_kv_dev, c->local_cap_dev};
   for (void* p : bufs)
     if (p) cudaFree(p);
   delete c;
@@ -343,7 +356,10 @@ okv_status okv_create(const okv_config* cfg, okv_ctx** out) {
             alloc((void**)&c->ctr_dev, sizeof(Counters)) &&
             alloc((void**)&c->draft_buf, (size_t)L * G.R * G.Hq * G.d * G.elem) &&
             alloc((void**)&c->scores, (size_t)U * G.nb_max * sizeof(uint32_t)) &&
-            alloc((void**)&c->stage_arrivals, (size_t)U * 4) && alloc((void**)&c->attend_arrivals, (size_t)U * 4);
+            alloc((void**)&c->stage_arrivals, (size_t)U * 4) && alloc((void**)&c->attend_arrivals, (size_t)U * 4) &&
+            alloc((void**)&c->local_of, (size_t)L * U * G.nb_max * 4) && alloc((void**)&c->local_used, (size_t)L * U * 4) &&
+            alloc((void**)&c->route, (size_t)L * U * G.kb * 4) && alloc((void**)&c->local_kv_dev, G.R * 8) &&
+            alloc((void**)&c->local_cap_dev, G.R * 4);
   if (ok) {
     size_t ws = 0;
     for (int32_t n = 1; n <= G.R; ++n) {
@@ -372,6 +388,11 @@ okv_status okv_create(const okv_config* cfg, okv_ctx** out) {
   ck(cudaMemset(c->ctr_dev, 0, sizeof(Counters)));
   ck(cudaMemset(c->host_kv_dev, 0, G.R * 8));
   ck(cudaMemset(c->cap_dev, 0, G.R * 4));
+  ck(cudaMemset(c->local_of, 0xFF, (size_t)L * U * G.nb_max * 4));
+  ck(cudaMemset(c->local_used, 0, (size_t)L * U * 4));
+  ck(cudaMemset(c->route, 0xFF, (size_t)L * U * G.kb * 4));
+  ck(cudaMemset(c->local_kv_dev, 0, G.R * 8));
+  ck(cudaMemset(c->local_cap_dev, 0xFF, G.R * 4));
   int lo = 0, hi = 0;
   ck(cudaDeviceGetStreamPriorityRange(&lo, &hi));
   // Scoring and selection run on the internal select stream at the least priority: they are
@@ -398,6 +419,8 @@ okv_status okv_create(const okv_config* cfg, okv_ctx** out) {
   c->active.assign(G.R, 0);
   c->host_ptr.assign(G.R, nullptr);
   c->cap_blocks.assign(G.R, 0);
+  c->local_ptr.assign(G.R, nullptr);
+  c->local_cap.assign(G.R, -1);
   c->len_host.assign((size_t)G.L * G.R, 0);
   c->shared_buf.assign(G.R, 0);
 
@@ -443,28 +466,67 @@ okv_status okv_create(const okv_config* cfg, okv_ctx** out) {
   return OKV_OK;
 }
 
-okv_status okv_add_request(okv_ctx* c, int32_t req, void* host_kv, int32_t capacity_blocks,
-                           int32_t n_tokens, void* stream) {
-  if (!c) return OKV_EINVAL;
-  const Geom& G = c->G;
-  cudaStream_t s = (cudaStream_t)stream;
-  if (req < 0 || req >= G.R) return fail(c, OKV_EINVAL, "okv_add_request: request id %d out of range", req);
-  if (c->active[req]) return fail(c, OKV_ESTATE, "okv_add_request: request %d is already active", req);
-  if (!host_kv) return fail(c, OKV_EINVAL, "okv_add_request: host_kv is NULL");
-  if (capacity_blocks <= 0 || capacity_blocks > G.nb_max)
-    return fail(c, OKV_EINVAL, "okv_add_request: capacity_blocks %d not in 1..%d", capacity_blocks, G.nb_max);
-  if (n_tokens < 0 || (int64_t)n_tokens > (int64_t)capacity_blocks * G.bs)
-    return fail(c, OKV_EINVAL, "okv_add_request: n_tokens %d exceeds the capacity", n_tokens);
-  // page-locked host memory only (on address-translation systems pageable memory would also be
-  // reachable, but at the mercy of the OS pager)
+}  // extern "C"
+
+namespace {
+
+// Device address of page-locked, device-mapped host memory, or nullptr.
+void* mapped_device_pointer(void* p) {
   cudaPointerAttributes attr{};
   void* dptr = nullptr;
-  if (cudaPointerGetAttributes(&attr, host_kv) != cudaSuccess || attr.type != cudaMemoryTypeHost ||
-      cudaHostGetDevicePointer(&dptr, host_kv, 0) != cudaSuccess || !dptr) {
+  // page-locked host memory only (on address-translation systems pageable memory would also be
+  // reachable, but at the mercy of the OS pager)
+  if (cudaPointerGetAttributes(&attr, p) != cudaSuccess || attr.type != cudaMemoryTypeHost ||
+      cudaHostGetDevicePointer(&dptr, p, 0) != cudaSuccess || !dptr) {
     cudaGetLastError();
-    return fail(c, OKV_EINVAL, "okv_add_request: host_kv is not page-locked, device-mapped memory");
+    return nullptr;
   }
-  if ((reinterpret_cast<uintptr_t>(dptr) & 15) != 0) return fail(c, OKV_EINVAL, "okv_add_request: host_kv must be 16-byte aligned");
+  return dptr;
+}
+
+bool overlaps(const void* a, int64_t na, const void* b, int64_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + (uintptr_t)nb && y < x + (uintptr_t)na;
+}
+
+// local_cap < 0: a request that holds its full KV (okv_add_request); else partial staging.
+okv_status add_request_impl(okv_ctx* c, const char* who, int32_t req, void* host_kv, int32_t capacity_blocks,
+                            void* local_kv, int32_t local_cap, int32_t n_tokens, void* stream) {
+  const Geom& G = c->G;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (req < 0 || req >= G.R) return fail(c, OKV_EINVAL, "%s: request id %d out of range", who, req);
+  if (c->active[req]) return fail(c, OKV_ESTATE, "%s: request %d is already active", who, req);
+  if (!host_kv) return fail(c, OKV_EINVAL, "%s: host_kv is NULL", who);
+  if (capacity_blocks <= 0 || capacity_blocks > G.nb_max)
+    return fail(c, OKV_EINVAL, "%s: capacity_blocks %d not in 1..%d", who, capacity_blocks, G.nb_max);
+  if (n_tokens < 0 || (int64_t)n_tokens > (int64_t)capacity_blocks * G.bs)
+    return fail(c, OKV_EINVAL, "%s: n_tokens %d exceeds the capacity", who, n_tokens);
+  void* dptr = mapped_device_pointer(host_kv);
+  if (!dptr) return fail(c, OKV_EINVAL, "%s: host_kv is not page-locked, device-mapped memory", who);
+  if ((reinterpret_cast<uintptr_t>(dptr) & 15) != 0) return fail(c, OKV_EINVAL, "%s: host_kv must be 16-byte aligned", who);
+  const int64_t unit_bytes = (int64_t)G.L * G.Hkv * G.block_bytes;
+  void* lptr = nullptr;
+  if (local_cap >= 0) {
+    if (local_cap > capacity_blocks)
+      return fail(c, OKV_EINVAL, "%s: local_capacity_blocks %d not in 0..%d", who, local_cap, capacity_blocks);
+    if (local_cap > 0) {
+      if (!local_kv) return fail(c, OKV_EINVAL, "%s: local_kv is NULL", who);
+      lptr = mapped_device_pointer(local_kv);
+      if (!lptr) return fail(c, OKV_EINVAL, "%s: local_kv is not page-locked, device-mapped memory", who);
+      if ((reinterpret_cast<uintptr_t>(lptr) & 15) != 0)
+        return fail(c, OKV_EINVAL, "%s: local_kv must be 16-byte aligned", who);
+      const int64_t lbytes = unit_bytes * local_cap;
+      bool clash = overlaps(local_kv, lbytes, host_kv, unit_bytes * capacity_blocks);
+      for (int32_t r : c->active_list) {
+        clash = clash || overlaps(local_kv, lbytes, c->host_ptr[r], unit_bytes * c->cap_blocks[r]);
+        if (c->local_cap[r] > 0) clash = clash || overlaps(local_kv, lbytes, c->local_ptr[r], unit_bytes * c->local_cap[r]);
+      }
+      if (clash) return fail(c, OKV_EINVAL, "%s: local_kv overlaps a buffer of an active request", who);
+    }
+  }
+  for (int32_t r : c->active_list)
+    if (c->local_cap[r] > 0 && overlaps(host_kv, unit_bytes * capacity_blocks, c->local_ptr[r], unit_bytes * c->local_cap[r]))
+      return fail(c, OKV_EINVAL, "%s: host_kv overlaps the decode-side tier of request %d", who, r);
   // every earlier use of the context's tables must be complete before they are reset
   if (okv_status st = sync_internal(c)) return st;
   OKV_CUDA(c, cudaStreamSynchronize(s));
@@ -480,8 +542,26 @@ okv_status okv_add_request(okv_ctx* c, int32_t req, void* host_kv, int32_t capac
       break;
     }
   }
-  OKV_CUDA(c, okv::launch_reset_request(G, c->slot_block, c->stamp, c->n_sel, c->n_fetch, c->len, req, n_tokens,
-                                        (uint64_t)(uintptr_t)dptr, capacity_blocks, c->host_kv_dev, c->cap_dev, s));
+  okv::StateBase B;
+  B.slot_block = c->slot_block;
+  B.stamp = c->stamp;
+  B.n_sel = c->n_sel;
+  B.n_fetch = c->n_fetch;
+  B.len = c->len;
+  B.local_of = c->local_of;
+  B.local_used = c->local_used;
+  B.host_kv_tab = c->host_kv_dev;
+  B.local_kv_tab = c->local_kv_dev;
+  B.cap_tab = c->cap_dev;
+  B.local_cap_tab = c->local_cap_dev;
+  okv::RequestInit q;
+  q.req = req;
+  q.n_tok = n_tokens;
+  q.cap = capacity_blocks;
+  q.local_cap = local_cap;
+  q.host_kv = (uint64_t)(uintptr_t)dptr;
+  q.local_kv = (uint64_t)(uintptr_t)lptr;
+  OKV_CUDA(c, okv::launch_reset_request(G, B, q, s));
   c->launches += 1;
   if (twin >= 0) {
     const size_t bytes = (size_t)G.Hkv * G.nb_max * 2 * G.d * G.elem;
@@ -500,9 +580,30 @@ okv_status okv_add_request(okv_ctx* c, int32_t req, void* host_kv, int32_t capac
   c->active[req] = 1;
   c->host_ptr[req] = host_kv;
   c->cap_blocks[req] = capacity_blocks;
+  c->local_ptr[req] = local_cap > 0 ? local_kv : nullptr;
+  c->local_cap[req] = local_cap;
   for (int32_t l = 0; l < G.L; ++l) c->len_host[(size_t)l * G.R + req] = n_tokens;
   if (okv_status st = upload_active(c)) return st;
   return check_device_error(c);
+}
+
+}  // namespace
+
+extern "C" {
+
+okv_status okv_add_request(okv_ctx* c, int32_t req, void* host_kv, int32_t capacity_blocks,
+                           int32_t n_tokens, void* stream) {
+  if (!c) return OKV_EINVAL;
+  return add_request_impl(c, "okv_add_request", req, host_kv, capacity_blocks, nullptr, -1, n_tokens, stream);
+}
+
+okv_status okv_add_request_partial(okv_ctx* c, int32_t req, void* full_kv, int32_t capacity_blocks,
+                                   void* local_kv, int32_t local_capacity_blocks, int32_t n_tokens, void* stream) {
+  if (!c) return OKV_EINVAL;
+  if (local_capacity_blocks < 0)
+    return fail(c, OKV_EINVAL, "okv_add_request_partial: local_capacity_blocks %d is negative", local_capacity_blocks);
+  return add_request_impl(c, "okv_add_request_partial", req, full_kv, capacity_blocks, local_kv,
+                          local_capacity_blocks, n_tokens, stream);
 }
 
 okv_status okv_remove_request(okv_ctx* c, int32_t req) {
@@ -513,6 +614,8 @@ okv_status okv_remove_request(okv_ctx* c, int32_t req) {
   OKV_CUDA(c, cudaDeviceSynchronize());
   c->active[req] = 0;
   c->host_ptr[req] = nullptr;
+  c->local_ptr[req] = nullptr;
+  c->local_cap[req] = -1;
   for (int32_t l = 0; l < c->G.L; ++l) c->len_host[(size_t)l * c->G.R + req] = 0;
   return upload_active(c);
 }
@@ -789,6 +892,19 @@ okv_status okv_read_lengths(okv_ctx* c, int32_t layer, int32_t* lengths) {
   return check_device_error(c);
 }
 
+okv_status okv_read_local(okv_ctx* c, int32_t layer, int32_t* local_used, int32_t* local_of, int32_t* routes) {
+  if (!c) return OKV_EINVAL;
+  const Geom& G = c->G;
+  if (layer < 0 || layer >= G.L) return fail(c, OKV_EINVAL, "okv_read_local: layer out of range");
+  if (okv_status st = sync_internal(c)) return st;
+  const LayerState S = layer_state(c, layer);
+  const int64_t U = c->per_layer_units;
+  if (local_used) OKV_CUDA(c, cudaMemcpy(local_used, S.local_used, U * 4, cudaMemcpyDeviceToHost));
+  if (local_of) OKV_CUDA(c, cudaMemcpy(local_of, S.local_of, U * G.nb_max * 4, cudaMemcpyDeviceToHost));
+  if (routes) OKV_CUDA(c, cudaMemcpy(routes, S.route, U * G.kb * 4, cudaMemcpyDeviceToHost));
+  return check_device_error(c);
+}
+
 okv_status okv_set_timing(okv_ctx* c, int32_t enable) {
   if (!c) return OKV_EINVAL;
   if (okv_status st = sync_internal(c)) return st;
@@ -826,6 +942,9 @@ okv_status okv_read_timing(okv_ctx* c, okv_timing* out) {
   }
   out->fetched_blocks = (int64_t)h.fetched_blocks;
   out->attended_slots = (int64_t)h.attended_slots;
+  out->local_hits = (int64_t)h.local_hits;
+  out->local_fills = (int64_t)h.local_fills;
+  out->full_reads = (int64_t)h.full_reads;
   return OKV_OK;
 }
 

@@ -20,6 +20,7 @@ enum DeviceError : int32_t {
   kErrCapacity = 3,     // an append past the request's host capacity
   kErrLength = 4,       // a context length outside [0, max_blocks * block_size]
   kErrTimeout = 5,      // a bounded wait for an asynchronous copy gave up
+  kErrLocalRange = 6,   // a decode-side tier entry outside [0, local_cap)
 };
 
 // Geometry shared by host and kernels (passed by value).
@@ -42,6 +43,11 @@ struct LayerState {
   int32_t* fetch;       // [R][Hkv][kb][2] (block, slot)
   int32_t* n_fetch;     // [R][Hkv]
   int32_t* len;         // [R] tokens of each request at this layer
+  // decode-side tier of partially staged requests
+  int32_t* local_of;    // [R][Hkv][nb_max] block -> kept entry or -1
+  int32_t* local_used;  // [R][Hkv] entries in use
+  int32_t* route;       // [R][Hkv][kb] per fetch entry: 2e = read kept entry e, 2e+1 = read the
+                        // full copy and keep it in entry e, -1 = read the full copy only
 };
 
 // Per-request device-side tables (shared by all layers).
@@ -49,11 +55,16 @@ struct ReqTables {
   const int32_t* active;    // [n_active] compact list of active request ids
   const uint64_t* host_kv;  // [R] device address of the request's host KV buffer
   const int32_t* cap_blocks;// [R]
+  const uint64_t* local_kv; // [R] device address of the decode-side tier, 0 for none
+  const int32_t* local_cap; // [R] entries per unit of the decode-side tier; -1: full-KV request
 };
 
 struct Counters {
   unsigned long long fetched_blocks;
   unsigned long long attended_slots;
+  unsigned long long local_hits;   // fetches of partially staged requests served by a kept copy
+  unsigned long long local_fills;  // ... read from the full copy and kept
+  unsigned long long full_reads;   // ... read from the full copy (fills included)
 };
 
 // ---- kernel launchers (defined in the k_*.cu files) --------------------------------------
@@ -66,10 +77,18 @@ cudaError_t launch_summary_build(const Geom& G, int32_t layer_begin, int32_t lay
 cudaError_t launch_append(const Geom& G, const LayerState& S, const ReqTables& T, int32_t n_active,
                           int32_t layer, const void* k_new, const void* v_new, int32_t* err,
                           cudaStream_t s);
-cudaError_t launch_reset_request(const Geom& G, int32_t* slot_block, int32_t* stamp, int32_t* n_sel,
-                                 int32_t* n_fetch, int32_t* len, int32_t req, int32_t n_tok,
-                                 uint64_t host_kv, int32_t cap, uint64_t* host_kv_tab, int32_t* cap_tab,
-                                 cudaStream_t s);
+// Empties request `req`'s pool, tables and decode-side tier on every layer and records its
+// buffers (local_cap -1 and local_kv 0 for a request that holds its full KV).
+struct RequestInit {
+  int32_t req, n_tok, cap, local_cap;
+  uint64_t host_kv, local_kv;
+};
+struct StateBase {  // whole-context arrays, [layers] x per-layer block
+  int32_t *slot_block, *stamp, *n_sel, *n_fetch, *len, *local_of, *local_used;
+  uint64_t *host_kv_tab, *local_kv_tab;
+  int32_t *cap_tab, *local_cap_tab;
+};
+cudaError_t launch_reset_request(const Geom& G, const StateBase& B, const RequestInit& q, cudaStream_t s);
 cudaError_t launch_advance(const LayerState& S, const ReqTables& T, int32_t n_active, cudaStream_t s);
 // Staging of one layer for every active unit: block scores (into `scores`, a [R][Hkv][nb_max]
 // uint32 workspace) by chunks of blocks; the last chunk of each unit to finish (counted in

@@ -6,7 +6,9 @@ Comparison rules (the method's tolerances):
   1e-6 * |s_K| of the K-th score s_K (binary32 scores summed in different orders may
   order such near-ties differently); after an accepted selection the oracle's KV
   selection step is re-synced to the GPU's selection so later state compares exactly;
-* attention: max abs error <= 1e-5 (binary32 storage) or 2e-2 (bfloat16 storage).
+* attention: max abs error <= 1e-5 (binary32 storage) or 2e-2 (bfloat16 storage);
+* decode-side tiers of partially staged requests (routes, entries in use, kept entry of each
+  block): exact; kept copies equal their blocks of the full copy byte for byte.
 """
 from __future__ import annotations
 
@@ -41,7 +43,7 @@ def out_to_f64(t, dtype) -> np.ndarray:
 
 class Rig:
     def __init__(self, w: synth.Workload, *, contexts=None, capacity_tokens=None, n_alias=None,
-                 max_requests=None, active=None, layers_kept=None, n_threads=None):
+                 max_requests=None, active=None, layers_kept=None, n_threads=None, local_cap=None):
         self.w = w
         B = w.batch
         self.contexts = np.asarray(contexts if contexts is not None else w.contexts(), np.int32)
@@ -71,17 +73,32 @@ class Rig:
                               plant_blocks=nb_plant)
                 self.bufs[k] = hb
         self.ctx = Context(self.cfg)
+        # local_cap[i] >= 0: batch request i is partially staged with that many decode-side
+        # entries per unit (a buffer of its own); -1: it holds its full KV
+        self.local_cap = np.full(B, -1, np.int32) if local_cap is None else \
+            np.array(np.broadcast_to(np.asarray(local_cap, np.int32), (B,)))
+        self.local_bufs = {}
         for i in range(B):
-            self.ctx.add_request(int(self.ids[i]), self.bufs[int(self.keys[i])].ptr, self.cap_blocks,
-                                 int(self.contexts[i]))
+            full = self.bufs[int(self.keys[i])].ptr
+            if self.local_cap[i] < 0:
+                self.ctx.add_request(int(self.ids[i]), full, self.cap_blocks, int(self.contexts[i]))
+                continue
+            lb = None
+            if self.local_cap[i] > 0:
+                lb = HostBuffer(self.cfg.host_bytes(int(self.local_cap[i])))
+                self.local_bufs[i] = lb
+            self.ctx.add_request_partial(int(self.ids[i]), full, self.cap_blocks, lb.ptr if lb else 0,
+                                         int(self.local_cap[i]), int(self.contexts[i]))
         # the oracle sees request slot i of the batch (rows of the device arrays = request ids)
         self.model = oracle.OracleModel(
             layers=w.layers, q_heads=w.q_heads, kv_heads=w.kv_heads, head_dim=w.head_dim,
             block_size=w.block_size, budget_tokens=w.budget_tokens, dtype=w.dtype,
             req_ptrs=[self.bufs[int(k)].ptr for k in self.keys],
             cap_blocks=[self.cap_blocks] * B, n_tok=self.contexts, n_threads=n_threads,
-            layers_kept=layers_kept)
+            layers_kept=layers_kept, local_cap=self.local_cap)
         self.sdt = np.float32 if w.dtype == F32 else np.uint16
+        # the oracle's routes of partially staged requests, summed over every staging checked
+        self.tally = {"local_hits": 0, "local_fills": 0, "full_reads": 0}
         self._summarised = set()  # (layer, batch index) whose oracle summaries are built
 
     def _ensure_summaries(self, layer: int, requests=None) -> None:
@@ -165,6 +182,49 @@ class Rig:
                 assert np.array_equal(entries[r, h, :n], self.model.fetch[layer][i, h, :n]), \
                     f"fetch list: layer {layer} req {i} head {h}"
 
+    def check_local(self, layer: int, requests=None) -> None:
+        """Decode-side tiers: routes, entries in use and kept entries exactly as the oracle's;
+        every kept copy equal to its block of the full copy over the block's valid tokens."""
+        used, local_of, routes = self.ctx.read_local(layer)
+        counts, _ = self.ctx.read_fetch_list(layer)
+        reqs = range(self.w.batch) if requests is None else requests
+        bs, nbm = self.w.block_size, self.cap_blocks
+        for i in reqs:
+            r = int(self.ids[i])
+            for h in range(self.w.kv_heads):
+                n = int(counts[r, h])
+                assert np.array_equal(routes[r, h, :n], self.model.route[layer][i, h, :n]), \
+                    f"routes: layer {layer} req {i} head {h}: {routes[r, h, :n]} vs {self.model.route[layer][i, h, :n]}"
+            if self.local_cap[i] < 0:
+                continue
+            assert np.array_equal(used[r], self.model.local_used[layer][i]), f"entries in use: layer {layer} req {i}"
+            assert np.array_equal(local_of[r][:, :nbm], self.model.local_of[layer][i][:, :nbm]), \
+                f"kept entries: layer {layer} req {i}"
+            if self.local_cap[i] == 0:
+                continue
+            lc = int(self.local_cap[i])
+            kept = self.local_bufs[i].numpy(self.sdt, (self.w.layers, self.w.kv_heads, lc, 2, bs, self.w.head_dim))
+            n_tok = int(self.model.n_tok[layer, i])
+            for h in range(self.w.kv_heads):
+                full = self.model.host_unit(layer, i, h)
+                for b in np.nonzero(local_of[r, h, :nbm] >= 0)[0]:
+                    e = int(local_of[r, h, b])
+                    nv = min(bs, n_tok - int(b) * bs)
+                    assert np.array_equal(kept[layer, h, e, :, :nv], full[b, :, :nv]), \
+                        f"kept copy differs: layer {layer} req {i} head {h} block {b} entry {e}"
+
+    def _tally_routes(self, layer: int, requests=None) -> None:
+        for i in (range(self.w.batch) if requests is None else requests):
+            if self.local_cap[i] < 0:
+                continue
+            for h in range(self.w.kv_heads):
+                rt = self.model.route[layer][i, h, :int(self.model.n_fetch[layer][i, h])]
+                hits = int(((rt >= 0) & ((rt & 1) == 0)).sum())
+                fills = int(((rt >= 0) & ((rt & 1) == 1)).sum())
+                self.tally["local_hits"] += hits
+                self.tally["local_fills"] += fills
+                self.tally["full_reads"] += len(rt) - hits
+
     def check_pool(self, layer: int, requests=None, heads=None) -> None:
         sb, _ = self.ctx.read_slot_table(layer)
         reqs = range(self.w.batch) if requests is None else requests
@@ -207,6 +267,8 @@ class Rig:
         C = oracle.fetch_cap_blocks(cap, self.kb)
         self.model.select(layer, C, step, sel_override=gsel, requests=requests)
         self.check_tables(layer, requests=requests)
+        self.check_local(layer, requests=requests)
+        self._tally_routes(layer, requests)
         if check_pool:
             self.check_pool(layer, requests=requests)
         return swaps
@@ -251,4 +313,6 @@ class Rig:
     def close(self):
         self.ctx.close()
         for b in self.bufs.values():
+            b.free()
+        for b in self.local_bufs.values():
             b.free()

@@ -34,10 +34,29 @@ def test_library_exports_every_declared_symbol(lib):
     assert not missing, missing
 
 
-def test_struct_layouts(lib):
+def test_struct_layouts(lib, tmp_path):
+    """The binding's ctypes mirrors of okv_config and okv_timing match the header as a C
+    compiler lays it out (sizes and every field offset)."""
+    import subprocess
     from sparse_kv_cache_draft_gb300 import binding
-    assert ctypes.sizeof(binding._Config) == 40
-    assert ctypes.sizeof(binding._Timing) == 7 * 8 + 7 * 8 + 8 + 8
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    fields = {"okv_config": binding._Config, "okv_timing": binding._Timing}
+    lines = ['#include <stddef.h>', '#include <stdio.h>', '#include "okv.h"', "int main(void) {"]
+    for cname, py in fields.items():
+        lines.append(f'  printf("{cname} %zu\\n", sizeof({cname}));')
+        for f, _ in py._fields_:
+            lines.append(f'  printf("{cname}.{f} %zu\\n", offsetof({cname}, {f}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c99", "-I", inc, "-o", str(exe), str(src)], check=True)
+    got = dict(l.split() for l in subprocess.run([str(exe)], check=True, capture_output=True,
+                                                  text=True).stdout.splitlines())
+    for cname, py in fields.items():
+        assert int(got[cname]) == ctypes.sizeof(py), cname
+        for f, _ in py._fields_:
+            assert int(got[f"{cname}.{f}"]) == getattr(py, f).offset, (cname, f)
 
 
 def test_status_strings(lib):
