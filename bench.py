@@ -58,10 +58,11 @@ def parse_args():
     p.add_argument("--batch", type=int, default=0, help="override the batch (smaller profiling cases)")
     p.add_argument("--layers", type=int, default=0, help="override the layer count (smaller profiling cases)")
     p.add_argument("--baseline-layers", type=int, default=6, help="layers in the cpu_baseline sample")
-    p.add_argument("--report", choices=["bench", "capsweep", "agreement", "dense"], default="bench",
+    p.add_argument("--report", choices=["bench", "capsweep", "agreement", "dense", "partial"], default="bench",
                    help="capsweep: bytes per step and tok/s per fetch cap (batch-90 sweep workload); "
                         "agreement: draft vs previous-token top-K agreement with the true next query; "
-                        "dense: dense decode attention over the full KV in HBM vs the sparse path, same shapes")
+                        "dense: dense decode attention over the full KV in HBM vs the sparse path, same shapes; "
+                        "partial: admission-time partial staging traffic, occupancy and tok/s at 24K and 32K")
     p.add_argument("--workload", default=None, help="synthetic workload name (default: the metric's)")
     return p.parse_args()
 
@@ -716,6 +717,100 @@ def run_dense(args, dist: Dist):
             "peak_source": f"hbm_gbs, {src}"}
 
 
+def run_partial(args, dist: Dist):
+    """Admission-time partial staging: bytes that cross from the full copy (the prefill side's
+    host memory) to the decode side at admission and during decoding, the decode side's host
+    occupancy, and decode tok/s against the same steps on requests that hold their full KV."""
+    import torch
+    from sparse_kv_cache_draft_gb300 import Context, HostBuffer
+    names = [args.workload] if args.workload else ["qwen3_8b_pd_24k_b8", "qwen3_8b_pd_32k_b8"]
+    S = args.steps
+    marks = sorted({m for m in (16, 64, 256) if m < S} | {S})
+    results = []
+    for name in names:
+        # the full copies are only read: a few buffers stand for the batch's prefill-side memory
+        wl = Workload(min(args.alias, 4), args.threads, args.batch, args.layers, name)
+        bufs = wl.host_kv()
+        L, B, Hkv, nb, kb, d, bs = wl.L, wl.B, wl.Hkv, wl.nb, wl.kb, wl.d, wl.w.block_size
+        block_bytes = 2 * bs * d * 2
+        full_bytes = L * Hkv * nb * block_bytes      # one request's KV: what a full admission moves
+        summ_bytes = L * Hkv * nb * 2 * d * 2        # its min/max summaries
+        q, dr = _device_inputs(wl, S)
+        out = torch.empty(q.shape[1:], dtype=torch.bfloat16, device="cuda")
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        rows = []
+        for cap in wl.w.caps:
+            C = max(1, min(kb, int(cap * kb)))
+            lcap = min(nb, kb + C * S)  # room for every block the run can demand: nothing bypasses
+            cfg = wl.config()
+            cfg.fetch_cap = cap
+            local = [HostBuffer(cfg.host_bytes(lcap)) for _ in range(B)]
+            ctx = Context(cfg)
+            for r in range(B):
+                ctx.add_request_partial(r, bufs[int(wl.keys[r])].ptr, nb, local[r].ptr, lcap, wl.n_tok)
+            ctx.set_timing(True)
+            for l in range(L):
+                ctx.stage(l, dr[0, l], 0, 1.0)
+            adm = ctx.read_timing()
+            ctx.set_timing(True)
+            ms, done, curve = 0.0, 0, []
+            for m in marks:
+                e0.record()
+                for t in range(done, m):
+                    ctx.step(q[t], dr[t + 1], out, t + 1)
+                done = m
+                ctx.join()
+                e1.record()
+                e1.synchronize()
+                ms += e0.elapsed_time(e1)
+                tm = ctx.read_timing()
+                dec_bytes = tm["full_reads"] * block_bytes / B
+                total = summ_bytes + adm["full_reads"] * block_bytes / B + dec_bytes
+                curve.append({"steps": m, "decode_gb_per_request": round(dec_bytes / 1e9, 4),
+                              "total_reduction": round(full_bytes / total, 3),
+                              "local_hit_frac": round(tm["local_hits"] / max(1, tm["fetched_blocks"]), 4)})
+            kept = sum(int(ctx.read_local(l)[0][:B].sum()) for l in range(L))
+            passed = tm["full_reads"] - tm["local_fills"] + adm["full_reads"] - adm["local_fills"]
+            ctx.close()
+            for b in local:
+                b.free()
+            partial_tok = B * S / (ms / 1e3)
+            # the same steps with every request holding its full KV
+            ctx = _setup_context(wl, bufs, cap)
+            ctx.set_timing(True)
+            for l in range(L):
+                ctx.stage(l, dr[0, l], 0, 1.0)
+            torch.cuda.synchronize()
+            e0.record()
+            for t in range(S):
+                ctx.step(q[t], dr[t + 1], out, t + 1)
+            ctx.join()
+            e1.record()
+            e1.synchronize()
+            full_tok = B * S / (e0.elapsed_time(e1) / 1e3)
+            ctx.close()
+            adm_bytes = summ_bytes + adm["full_reads"] * block_bytes / B
+            rows.append({
+                "fetch_cap": cap, "C_blocks": C, "decode_steps": S, "decode_side_entries_per_unit": lcap,
+                "full_kv_gb_per_request": round(full_bytes / 1e9, 4),
+                "admission_gb_per_request": round(adm_bytes / 1e9, 4),
+                "admission_summary_gb": round(summ_bytes / 1e9, 4),
+                "admission_reduction": round(full_bytes / adm_bytes, 3),
+                "curve": curve,
+                "decode_side_occupancy_gb_per_request": round(kept * block_bytes / B / 1e9, 4),
+                "occupancy_reduction": round(full_bytes / max(1, kept * block_bytes / B), 3),
+                "bypassed_blocks": int(passed),
+                "partial_tok_s": round(partial_tok, 1), "full_kv_tok_s": round(full_tok, 1)})
+        for b in bufs:
+            b.free()
+        del q, dr, out
+        torch.cuda.empty_cache()
+        results.append({"workload": name, "context": wl.n_tok, "batch": B, "rows": rows})
+    return {"report": "partial", "metric": "admission-time partial staging: full-copy -> decode-side traffic, "
+            "decode-side occupancy and tok/s", "unit": "GB per request", "n_gpus": dist.world, "steps": S,
+            "data": "synthetic", "workloads": results}
+
+
 def main():
     args = parse_args()
     dist = Dist(want_gpu=args.impl == "okv")
@@ -726,6 +821,8 @@ def main():
             res = run_agreement(args, dist) if dist.rank == 0 else None
         elif args.report == "dense":
             res = run_dense(args, dist) if dist.rank == 0 else None
+        elif args.report == "partial":
+            res = run_partial(args, dist) if dist.rank == 0 else None
         else:
             res = run_okv(args, dist) if args.impl == "okv" else run_reference(args, dist)
         if res is not None and dist.rank == 0:

@@ -161,6 +161,15 @@ WORKLOADS = {
                                       kv_heads=8, head_dim=128, batch=90, context=16384,
                                       steps=16, n_dirs=100, n_active=5,
                                       caps=(0.01, 0.02, 0.05, 0.1, 0.25, 1.0)),
+    # admission-time partial staging at the disaggregated-serving contexts (24K and 32K): the
+    # cap-sweep structure (100 directions at 1% of blocks, 5 active, one replaced per step), so
+    # decode-time demand keeps drifting to blocks the admission did not stage
+    "qwen3_8b_pd_24k_b8": Workload("qwen3_8b_pd_24k_b8", seed=6, layers=36, q_heads=32, kv_heads=8,
+                                   head_dim=128, batch=8, context=24576, steps=256, n_dirs=100,
+                                   n_active=5, caps=(0.05, 1.0)),
+    "qwen3_8b_pd_32k_b8": Workload("qwen3_8b_pd_32k_b8", seed=7, layers=36, q_heads=32, kv_heads=8,
+                                   head_dim=128, batch=8, context=32768, steps=256, n_dirs=100,
+                                   n_active=5, caps=(0.05, 1.0)),
 }
 
 

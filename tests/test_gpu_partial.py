@@ -103,3 +103,56 @@ def test_partial_staging_api_errors():
         full.free()
         local.free()
         local2.free()
+
+
+def test_pd_32k_b8_full_size_sampled():
+    """The partial-staging report's 32K workload at full size (36 layers, batch 8, 2048 blocks per
+    unit, 4 full copies aliased, tiers of Kb + 256 C = 1664 entries), driven as the report drives
+    it: a cap-1.0 bootstrap, then decode steps through okv_step at cap 0.05. Layers 0 and 35 of
+    requests 0, 3 and 7 are followed by the oracle: selections, tables, routes, tiers, kept bytes,
+    pools and attention."""
+    import torch
+    import oracle
+    from okv_harness import to_device, torch_dtype
+    w = synth.WORKLOADS["qwen3_8b_pd_32k_b8"]
+    layers, sample = [0, 35], [0, 3, 7]
+    C = oracle.fetch_cap_blocks(w.fetch_cap, w.budget_tokens // w.block_size)
+    nb = w.context // w.block_size
+    lcap = min(nb, w.budget_tokens // w.block_size + C * 256)
+    rig = Rig(w, n_alias=4, layers_kept=layers, local_cap=lcap)
+    try:
+        L, R, Hq, d = w.layers, rig.R, w.q_heads, w.head_dim
+
+        def all_layers(step, kind):
+            return np.stack([rig.batch_queries(l, step, kind) for l in range(L)])
+
+        def stage_check(layer, draft, cap_blocks, stamp):
+            rig._ensure_summaries(layer, sample)
+            rig.model.score_topk(layer, draft, requests=sample)
+            gsel, _ = rig.check_selection(layer, requests=sample)
+            rig.model.select(layer, cap_blocks, stamp, sel_override=gsel, requests=sample)
+            rig.check_tables(layer, requests=sample)
+            rig.check_local(layer, requests=sample)
+            rig.check_pool(layer, requests=sample, heads=[0, 7])
+
+        d_boot = all_layers(-1, 1)
+        for l in range(L):
+            rig.ctx.stage(l, to_device(d_boot[l], w.dtype), 0, 1.0)
+        torch.cuda.synchronize()
+        assert rig.ctx.sync(120_000) == 0
+        for l in layers:
+            stage_check(l, d_boot[l], oracle.fetch_cap_blocks(1.0, rig.kb), 0)
+        for t in range(3):
+            q = all_layers(t, 0)
+            dr = all_layers(t, 1)
+            out = torch.zeros((L, R, Hq, d), dtype=torch_dtype(w.dtype), device="cuda")
+            rig.ctx.step(to_device(q, w.dtype), to_device(dr, w.dtype), out, t + 1)
+            torch.cuda.synchronize()
+            assert rig.ctx.sync(120_000) == 0
+            for l in layers:
+                assert rig.check_attention(l, q[l], out[l], requests=sample) <= ATOL[w.dtype]
+                stage_check(l, dr[l], C, t + 1)
+        used, _, _ = rig.ctx.read_local(35)
+        assert used[:8].min() >= rig.kb and used[:8].max() <= rig.kb + 3 * C
+    finally:
+        rig.close()
