@@ -150,6 +150,9 @@ class Rig:
                 gsel = ids[r, h, :n]
                 osel = self.model.sel_ids[layer][i, h, :n]
                 osc = self.model.scores[layer][i, h, :nb]
+                g_cnt[i, h] = n
+                if n == 0:  # an empty context selects nothing
+                    continue
                 assert len(set(gsel.tolist())) == n and gsel.min() >= 0 and gsel.max() < nb
                 # GPU order: its own scores non-increasing, ties by block id
                 gs = scores[r, h, :n]
