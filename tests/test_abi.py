@@ -68,3 +68,14 @@ def test_null_context_is_rejected(lib):
     assert lib.okv_sync(None, 0) == 1
     assert lib.okv_attend(None, 0, None, None, None) == 1
     assert lib.okv_launch_count(None) == 0
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """Without libokv.so the binding raises instead of computing anything on the CPU."""
+    from sparse_kv_cache_draft_gb300 import Config, Context, binding
+    monkeypatch.setattr(binding, "library_path", lambda: str(tmp_path / "libokv.so"))
+    monkeypatch.setattr(binding, "_lib", None)
+    with pytest.raises(ImportError):
+        binding.load_library()
+    with pytest.raises(ImportError):
+        Context(Config(1, 8, 2, 64, 16, 512, 2, 8))
