@@ -4,7 +4,9 @@ okv_attend_static serves callers that cannot allocate device memory: it takes ev
 output from the caller and keeps its only workspace in a fixed array inside the library. Here
 a context stages real pools; their contents, slot tables and lengths are copied into caller
 tensors, and two calls in a row of the allocation-free entry point (two different queries)
-must agree with okv_attend on the same queries. This file is collected last on purpose.
+must agree with okv_attend on the same queries. The same entry point carries the dense
+baseline (every block of the full KV in HBM), checked against the oracle's dense attention.
+This file is collected last on purpose.
 """
 import numpy as np
 import pytest
@@ -66,3 +68,31 @@ def test_static_attention_rejects_oversized_shapes():
     assert L.okv_attend_static(243, 40, 5, 256, 16, 128, F32, p, p, p, p, p, None) == binding.EINVAL
     # a shape the attention does not take
     assert L.okv_attend_static(4, 6, 4, 128, 16, 128, BF16, p, p, p, p, p, None) == binding.EINVAL
+
+
+def test_dense_baseline_matches_oracle():
+    """The dense baseline (`bench.py --report dense`): okv_attend_static over an identity slot table
+    of every block (the full KV in HBM, 1024 slots per unit at 16K) equals the oracle's dense
+    softmax attention. Qwen3-8B attention shapes, one layer, contexts of 16384, 9000 and 1 tokens
+    (slots past a context hold -1)."""
+    import torch
+    w = synth.WORKLOADS["qwen3_8b_16k_b128"].scaled(layers=1, batch=3)
+    rig = Rig(w, contexts=[16384, 9000, 1])
+    try:
+        R, H, nb, bs, d = rig.R, w.kv_heads, rig.cap_blocks, w.block_size, w.head_dim
+        kv = np.stack([np.stack([rig.model.host_unit(0, i, h) for h in range(H)]) for i in range(R)])
+        pool = torch.from_numpy(np.ascontiguousarray(kv).view(np.int16)).view(torch.bfloat16).cuda()
+        sb = np.full((R, H, nb), -1, np.int32)
+        for i, n in enumerate(rig.contexts):
+            sb[i, :, :-(-int(n) // bs)] = np.arange(-(-int(n) // bs), dtype=np.int32)
+        lens = torch.from_numpy(rig.contexts.astype(np.int32)).cuda()
+        q = rig.batch_queries(0, 0, 0)
+        out = torch.full((R, w.q_heads, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+        binding.attend_static(pool, torch.from_numpy(sb).cuda(), lens, rig.device_rows(q, (w.q_heads, d)), out,
+                              q_heads=w.q_heads, kv_heads=H, head_dim=d, block_size=bs, slots=nb, dtype=BF16)
+        torch.cuda.synchronize()
+        want = rig.model.attend(0, q, dense=True)
+        err = float(np.abs(out_to_f64(out, BF16)[rig.ids] - want).max())
+        assert err <= ATOL[BF16], err
+    finally:
+        rig.close()
