@@ -328,7 +328,11 @@ def run_okv(args, dist: Dist):
 
     load_library()
     torch.cuda.set_device(dist.local)
-    wl = Workload(args.alias, args.threads, args.batch, args.layers, args.workload)
+    # ranks on one host share its memory and cores: each takes a share of the aliased host buffers
+    # (aliasing changes neither the device work nor the host-link bytes of a step)
+    alias = args.alias if dist.world == 1 else max(2, args.alias // dist.world)
+    threads = args.threads or (max(1, (os.cpu_count() or 1) // dist.world) if dist.world > 1 else 0)
+    wl = Workload(alias, threads, args.batch, args.layers, args.workload)
     cfg = wl.config()
     B, L, Hq, d = wl.B, wl.L, wl.Hq, wl.d
     K, W = args.steps, args.warmup
