@@ -163,7 +163,8 @@ class ClockSampler:
 
 def profiled_traffic(profile: str):
     """DRAM bytes per launch recorded from an ncu capture in profiles/, or None once the kernel's
-    source has changed since the capture (the recorded sha256 prefix no longer matches)."""
+    sources have changed since the capture: the line names them (comma-separated) with the
+    sha256 prefix of their concatenated contents."""
     import hashlib
     import re
     try:
@@ -171,8 +172,10 @@ def profiled_traffic(profile: str):
         m = re.search(r"bench: traffic_bytes_per_launch=(\d+) source=(\S+) sha256_16=([0-9a-f]{16})", text)
         if not m:
             return None
-        src = open(os.path.join(ROOT, m.group(2)), "rb").read()
-        return int(m.group(1)) if hashlib.sha256(src).hexdigest()[:16] == m.group(3) else None
+        h = hashlib.sha256()
+        for path in m.group(2).split(","):
+            h.update(open(os.path.join(ROOT, path), "rb").read())
+        return int(m.group(1)) if h.hexdigest()[:16] == m.group(3) else None
     except OSError:
         return None
 
