@@ -324,6 +324,15 @@ def cpu_baseline(wl: Workload, bufs, n_layers=2):
 
 # ---- the okv arm -------------------------------------------------------------------------------
 
+def rank_host_share(alias: int, threads: int, world: int) -> tuple[int, int]:
+    """Host KV buffers and generator threads of one rank when `world` ranks share a host: each
+    rank aliases its share of the buffers (at least 2) and uses its share of the cores. Aliasing
+    changes neither the device work nor the host-link bytes of a step."""
+    if world <= 1:
+        return alias, threads
+    return max(2, alias // world), threads or max(1, (os.cpu_count() or 1) // world)
+
+
 def run_okv(args, dist: Dist):
     import numpy as np
     import torch
@@ -331,10 +340,7 @@ def run_okv(args, dist: Dist):
 
     load_library()
     torch.cuda.set_device(dist.local)
-    # ranks on one host share its memory and cores: each takes a share of the aliased host buffers
-    # (aliasing changes neither the device work nor the host-link bytes of a step)
-    alias = args.alias if dist.world == 1 else max(2, args.alias // dist.world)
-    threads = args.threads or (max(1, (os.cpu_count() or 1) // dist.world) if dist.world > 1 else 0)
+    alias, threads = rank_host_share(args.alias, args.threads, dist.world)
     wl = Workload(alias, threads, args.batch, args.layers, args.workload)
     cfg = wl.config()
     B, L, Hq, d = wl.B, wl.L, wl.Hq, wl.d

@@ -46,3 +46,14 @@ def test_two_ranks_barrier_and_max():
     got = sorted(q.get(timeout=5) for _ in range(2))
     assert [g[1] for g in got] == [2.5, 2.5]   # every rank sees the slowest rank's time
     assert got[1][2] is None                   # the reference arm runs on rank 0 only
+
+
+def test_ranks_share_the_host():
+    """Under torchrun the ranks on one host split its pinned KV buffers and its cores."""
+    import bench
+    assert bench.rank_host_share(16, 0, 1) == (16, 0)
+    assert bench.rank_host_share(16, 0, 2)[0] == 8
+    assert bench.rank_host_share(16, 0, 8)[0] == 2
+    assert bench.rank_host_share(16, 0, 16)[0] == 2
+    assert bench.rank_host_share(16, 3, 4) == (4, 3)
+    assert bench.rank_host_share(16, 0, 4)[1] >= 1
