@@ -60,7 +60,10 @@ typedef struct {
   int32_t block_size;             /* tokens per KV block (16) */
   int32_t budget_tokens;          /* KV budget per unit in tokens; Kb = budget/block_size slots */
   int32_t max_requests;           /* request ids are 0 .. max_requests-1 */
-  int32_t max_blocks_per_request; /* largest context (in blocks) any request may reach */
+  int32_t max_blocks_per_request; /* largest context (in blocks) any request may reach; the
+                                     selection keeps a unit's per-block arrays in one CTA's
+                                     shared memory, which bounds it (about 16000 blocks at a
+                                     128-slot budget on GB300; okv_create says the limit) */
   float fetch_cap;                /* default fetch cap, a fraction of the budget (0.05) */
   int32_t dtype;                  /* OKV_F32 or OKV_BF16 storage for KV, queries, outputs */
 } okv_config;

@@ -439,6 +439,12 @@ stage_kernel(Geom G, LayerState S, ReqTables RT, int32_t chunks, int32_t nb_cap,
 
 }  // namespace
 
+size_t stage_smem_bytes(const Geom& G, int32_t nb_cap) {
+  const size_t need_score = 16 + coef_bytes(G);
+  const size_t need_select = 16 + select_bytes(G, nb_cap > 0 ? nb_cap : 1);
+  return need_score > need_select ? need_score : need_select;
+}
+
 cudaError_t launch_stage(const Geom& G, const LayerState& S, const ReqTables& T, int32_t n_active,
                          int32_t max_nb, const void* draft, uint32_t* scores, int32_t* arrivals,
                          int32_t cap_blocks, int32_t step, Counters* ctr, int32_t* err, cudaStream_t s,
@@ -447,9 +453,7 @@ cudaError_t launch_stage(const Geom& G, const LayerState& S, const ReqTables& T,
   if (n_active <= 0) return cudaSuccess;
   const int32_t nb_cap = max_nb > 0 ? max_nb : 1;
   const int32_t chunks = (nb_cap + kScoreChunk - 1) / kScoreChunk;
-  const size_t need_score = 16 + coef_bytes(G);
-  const size_t need_select = 16 + select_bytes(G, nb_cap);
-  const size_t smem = need_score > need_select ? need_score : need_select;
+  const size_t smem = stage_smem_bytes(G, nb_cap);
   const int grid = n_active * G.Hkv * chunks;
   cudaError_t e;
   if (G.dtype == OKV_F32) {

@@ -329,6 +329,23 @@ okv_status okv_create(const okv_config* cfg, okv_ctx** out) {
   G.elem = k.dtype == OKV_F32 ? 4 : 2;
   G.block_bytes = (int64_t)2 * G.bs * G.d * G.elem;
   if ((G.bs * G.d * G.elem) % 16) return bad("block rows must be a multiple of 16 bytes");
+  {
+    // the selection of a unit runs in one CTA with the unit's per-block arrays on chip
+    int dev = 0, optin = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) optin = 0;
+    const size_t need = okv::stage_smem_bytes(G, G.nb_max);
+    if (optin > 0 && need > (size_t)optin) {
+      int32_t fits = G.nb_max;
+      while (fits > 1 && okv::stage_smem_bytes(G, fits) > (size_t)optin) fits -= fits > 4096 ? 64 : 1;
+      char why[256];
+      snprintf(why, sizeof(why),
+               "max_blocks_per_request %d needs %zu bytes of shared memory per staging CTA; this device "
+               "allows %d (at most about %d blocks at this budget)",
+               G.nb_max, need, optin, fits);
+      return bad(why);
+    }
+  }
 
   okv_status st = OKV_OK;
   auto alloc = [&](void** p, size_t bytes) -> bool {

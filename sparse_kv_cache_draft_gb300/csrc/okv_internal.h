@@ -95,6 +95,9 @@ cudaError_t launch_advance(const LayerState& S, const ReqTables& T, int32_t n_ac
 // `arrivals`, [R * Hkv] int32 that start at zero and are left at zero) runs the unit's top-K and
 // diff / admit / evict. One launch. With pred_ids / pred_n ([R][Hkv][Kb], [R][Hkv]) only the top-K
 // is computed, into them.
+// Dynamic shared memory of one staging CTA for contexts of up to nb_cap blocks: the selection
+// keeps per-block arrays of the unit (score images, block -> slot map, candidates) on chip.
+size_t stage_smem_bytes(const Geom& G, int32_t nb_cap);
 cudaError_t launch_stage(const Geom& G, const LayerState& S, const ReqTables& T, int32_t n_active,
                          int32_t max_nb, const void* draft, uint32_t* scores, int32_t* arrivals,
                          int32_t cap_blocks, int32_t step, Counters* ctr, int32_t* err, cudaStream_t s,

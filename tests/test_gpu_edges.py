@@ -98,3 +98,15 @@ def test_largest_budget_batch_one():
         assert counts[0].max() <= 51
     finally:
         rig.close()
+
+
+def test_longest_context_at_the_default_budget():
+    """256000 tokens (16000 blocks, near the largest context one staging CTA's shared memory
+    holds at a 128-slot budget), one request, cap 0.05."""
+    w = QWEN.scaled(layers=1, batch=1, context=256000)
+    rig = Rig(w)
+    try:
+        errs, _ = rig.run_steps(2, 0.05)
+        assert max(errs) <= ATOL[BF16]
+    finally:
+        rig.close()

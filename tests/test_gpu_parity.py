@@ -143,6 +143,9 @@ def test_api_errors():
         Context(Config(1, 6, 4, 128, 16, 2048, 2, 64))  # q heads not a multiple of kv heads
     with pytest.raises(OkvError):
         Context(Config(1, 8, 2, 100, 16, 2048, 2, 64))  # head_dim not a multiple of 32
+    with pytest.raises(OkvError) as e:  # the selection's on-chip arrays would exceed shared memory
+        Context(Config(1, 8, 2, 64, 16, 512, 1, 32767))
+    assert e.value.status == binding.EINVAL
     cfg = Config(1, 8, 2, 64, 16, 512, 2, 8, 1.0, F32)
     ctx = Context(cfg)
     hb = HostBuffer(cfg.host_bytes(8))
