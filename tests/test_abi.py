@@ -79,3 +79,23 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
         binding.load_library()
     with pytest.raises(ImportError):
         Context(Config(1, 8, 2, 64, 16, 512, 2, 8))
+
+
+def _build_c_demo(out_dir):
+    """Compile tests/c_abi_demo.c against include/okv.h and libokv.so (plain C99, CUDA runtime)."""
+    import subprocess
+    from sparse_kv_cache_draft_gb300 import library_path
+    cuda = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    lib_dir = os.path.dirname(library_path())
+    exe = os.path.join(str(out_dir), "c_abi_demo")
+    cmd = ["gcc", "-std=c99", "-O2", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+           "-I", os.path.join(cuda, "include"), os.path.join(ROOT, "tests", "c_abi_demo.c"), "-o", exe,
+           "-L", lib_dir, "-lokv", "-L", os.path.join(cuda, "lib64"), "-lcudart", "-lm",
+           f"-Wl,-rpath,{lib_dir}", f"-Wl,-rpath,{os.path.join(cuda, 'lib64')}"]
+    subprocess.run(cmd, check=True)
+    return exe
+
+
+def test_c_caller_compiles_and_links(lib, tmp_path):
+    """include/okv.h is plain C99 and a C program links against libokv.so with no Python or torch."""
+    assert os.path.exists(_build_c_demo(tmp_path))
