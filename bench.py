@@ -58,11 +58,12 @@ def parse_args():
     p.add_argument("--batch", type=int, default=0, help="override the batch (smaller profiling cases)")
     p.add_argument("--layers", type=int, default=0, help="override the layer count (smaller profiling cases)")
     p.add_argument("--baseline-layers", type=int, default=6, help="layers in the cpu_baseline sample")
-    p.add_argument("--report", choices=["bench", "capsweep", "agreement", "dense", "partial"], default="bench",
+    p.add_argument("--report", choices=["bench", "capsweep", "agreement", "dense", "partial", "append"], default="bench",
                    help="capsweep: bytes per step and tok/s per fetch cap (batch-90 sweep workload); "
                         "agreement: draft vs previous-token top-K agreement with the true next query; "
                         "dense: dense decode attention over the full KV in HBM vs the sparse path, same shapes; "
-                        "partial: admission-time partial staging traffic, occupancy and tok/s at 24K and 32K")
+                        "partial: admission-time partial staging traffic, occupancy and tok/s at 24K and 32K; "
+                        "append: the mixed-length workload with one appended token per request and layer")
     p.add_argument("--workload", default=None, help="synthetic workload name (default: the metric's)")
     return p.parse_args()
 
@@ -850,6 +851,96 @@ def run_partial(args, dist: Dist):
             "data": "synthetic", "workloads": results}
 
 
+def run_append(args, dist: Dist):
+    """Decode steps that append one token per request and layer: the mixed-length workload
+    (contexts ~ U[1K, 32K], one token per step), through okv_step with k_new / v_new. Appends go
+    to each request's own host buffer (requests sharing a buffer cannot append), so the batch is
+    32 by default to fit the host's memory."""
+    import numpy as np
+    import torch
+    import synth
+    from sparse_kv_cache_draft_gb300 import BF16, Config, Context, HostBuffer
+    name = args.workload or "qwen3_8b_mixed_b64"
+    w = synth.WORKLOADS[name].scaled(batch=args.batch or 32)
+    if args.layers:
+        w = w.scaled(layers=args.layers)
+    B, L, Hq, Hkv, d, bs = w.batch, w.layers, w.q_heads, w.kv_heads, w.head_dim, w.block_size
+    K, W = args.steps, args.warmup
+    n_steps = W + K
+    grow = max(1, w.grow_per_step)
+    ctx0 = w.contexts().astype(np.int64)
+    caps = [-(-(int(c) + grow * (n_steps + 1)) // bs) for c in ctx0]
+    cfg = Config(L, Hq, Hkv, d, bs, w.budget_tokens, B, max(caps), w.fetch_cap, BF16)
+    ids = np.arange(B, dtype=np.int32)
+    threads = args.threads or os.cpu_count() or 1
+    t0 = time.time()
+    bufs = [HostBuffer(cfg.host_bytes(caps[r])) for r in range(B)]
+    for r in range(B):
+        synth.fill_kv(bufs[r].ptr, w, r, 0, int(ctx0[r]), caps[r], n_threads=threads)
+    host_gb = sum(cfg.host_bytes(c) for c in caps) / 1e9
+    log(f"host KV: {B} own buffers, {host_gb:.1f} GB, in {time.time() - t0:.1f}s")
+    ctx = Context(cfg)
+    for r in range(B):
+        ctx.add_request(r, bufs[r].ptr, caps[r], int(ctx0[r]))
+    shape_q, shape_kv = (L, B, Hq, d), (L, B, Hkv, d)
+    qh = np.empty((n_steps,) + shape_q, np.uint16)
+    dh = np.empty((n_steps + 1,) + shape_q, np.uint16)
+    kh = np.empty((n_steps,) + shape_kv, np.uint16)
+    vh = np.empty_like(kh)
+    for t in range(-1, n_steps):
+        for l in range(L):
+            if t >= 0:
+                synth.queries(w, l, t, 0, ids, ids, out=qh[t, l], n_threads=threads)
+                kh[t, l], vh[t, l] = synth.token_kv(w, l, ids, ctx0 + t * grow)
+            synth.queries(w, l, t, 1, ids, ids, out=dh[t + 1, l], n_threads=threads)
+
+    def conv(a):
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to("cuda")
+
+    q, dr, kn, vn = conv(qh), conv(dh), conv(kh), conv(vh)
+    out = torch.empty(shape_q, dtype=torch.bfloat16, device="cuda")
+    for l in range(L):
+        ctx.stage(l, dr[0, l], 0, 1.0)
+    for t in range(W):
+        ctx.step(q[t], dr[t + 1], out, t + 1, k_new=kn[t], v_new=vn[t])
+    torch.cuda.synchronize()
+    assert ctx.sync(60_000) == 0
+    ctx.set_timing(True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for t in range(W, n_steps):
+        ctx.step(q[t], dr[t + 1], out, t + 1, k_new=kn[t], v_new=vn[t])
+    ctx.join()
+    e1.record()
+    e1.synchronize()
+    ms = dist.max(e0.elapsed_time(e1))
+    tm = ctx.read_timing()
+    assert ctx.sync(60_000) == 0
+    lens = ctx.read_lengths(0)[:B]
+    assert (lens == ctx0 + grow * n_steps).all(), "every request grew by one token per step"
+    hbm_peak, src = measured_peaks()
+    slot_bytes = 2 * bs * d * 2
+    nb_end = -(-(ctx0 + grow * n_steps) // bs)
+    summ_bytes = L * Hkv * int(nb_end.sum()) * 2 * d * 2  # per step, at the final lengths
+    att_bytes = tm["attended_slots"] / K * slot_bytes
+    step_ms = ms / K
+    ctx.close()
+    for b in bufs:
+        b.free()
+    return {"report": "append", "metric": "sparse-decode tok/s with one appended token per request and layer",
+            "unit": "tok/s", "n_gpus": dist.world, "steps": K, "warmup": W, "data": "synthetic",
+            "workload": f"{name} (batch {B}, {L} layers)", "contexts": {"min": int(ctx0.min()), "mean": float(ctx0.mean()),
+                                                                     "max": int(ctx0.max())},
+            "host_kv_gb": round(host_gb, 1),
+            "tok_s": round(dist.world * B * K / (ms / 1e3), 1), "ms_per_step": round(step_ms, 4),
+            "append_us_per_layer": round(tm["ms"]["append"] / (L * K) * 1e3, 2),
+            "append_share_of_step": round(tm["ms"]["append"] / K / step_ms, 4),
+            "step_hbm_gbs": round((att_bytes + summ_bytes) / (step_ms / 1e3) / 1e9, 1),
+            "step_hbm_frac": round((att_bytes + summ_bytes) / (step_ms / 1e3) / 1e9 / hbm_peak, 4),
+            "gather_gb_per_step": round(tm["fetched_blocks"] * slot_bytes / K / 1e9, 4),
+            "peak_source": f"hbm_gbs, {src}"}
+
+
 def main():
     args = parse_args()
     dist = Dist(want_gpu=args.impl == "okv")
@@ -862,6 +953,8 @@ def main():
             res = run_dense(args, dist) if dist.rank == 0 else None
         elif args.report == "partial":
             res = run_partial(args, dist) if dist.rank == 0 else None
+        elif args.report == "append":
+            res = run_append(args, dist) if dist.rank == 0 else None
         else:
             res = run_okv(args, dist) if args.impl == "okv" else run_reference(args, dist)
         if res is not None and dist.rank == 0:

@@ -75,65 +75,82 @@ __global__ void summary_build_kernel(Geom G, int32_t layer_begin, int32_t n_laye
   }
 }
 
-// grid (n_active, Hkv), one thread per dimension.
+// grid (n_active, Hkv), one thread per dimension. The last of a request's Hkv CTAs to finish
+// (counted in arrivals[r], which starts at zero and is left at zero) advances its length.
 template <typename T>
 __global__ void append_kernel(Geom G, LayerState S, ReqTables T_, int32_t layer,
                               const T* __restrict__ k_new, const T* __restrict__ v_new,
-                              int32_t* err) {
+                              int32_t* __restrict__ arrivals, int32_t* err) {
   const int32_t r = T_.active[blockIdx.x];
   const int32_t h = blockIdx.y;
   const int32_t pos = S.len[r];
   const int32_t cap = T_.cap_blocks[r];
-  if (pos < 0 || pos >= cap * G.bs || pos >= G.nb_max * G.bs) {
-    if (threadIdx.x == 0) record_error(err, kErrCapacity, layer, r, pos);
-    return;
-  }
-  const int32_t b = pos / G.bs, t = pos % G.bs;
-  const int64_t kofs = (int64_t)t * G.d, vofs = (int64_t)(G.bs + t) * G.d;
-  T* host = reinterpret_cast<T*>(T_.host_kv[r] +
-                                 (((int64_t)layer * G.Hkv + h) * cap + b) * G.block_bytes);
-  const int64_t unit = (int64_t)r * G.Hkv + h;
-  __shared__ int32_t tail_slot;  // slot holding the tail block, or -1
-  if (threadIdx.x == 0) tail_slot = -1;
-  __syncthreads();
-  for (int32_t s = threadIdx.x; s < G.kb; s += blockDim.x)
-    if (S.slot_block[unit * G.kb + s] == b) tail_slot = s;
-  __syncthreads();
-  const int32_t slot = tail_slot;
-  T* pool = slot >= 0 ? reinterpret_cast<T*>(S.pool + (unit * G.kb + slot) * G.block_bytes) : nullptr;
-  // a partially staged request also writes the decode side's kept copy of the block, if any
-  T* kept = nullptr;
   const int32_t lcap = T_.local_cap[r];
-  if (lcap > 0) {
-    const int32_t e = S.local_of[unit * G.nb_max + b];
-    if (e >= lcap) {
-      if (threadIdx.x == 0) record_error(err, kErrLocalRange, layer, r, e);
-      return;
+  const int64_t unit = (int64_t)r * G.Hkv + h;
+  __shared__ int32_t tail_slot;   // slot holding the tail block, or -1
+  __shared__ int32_t kept_entry;  // decode-side entry of the tail block (partial staging), or -1
+  __shared__ int32_t skip;        // a check failed: write nothing
+  if (threadIdx.x == 0) {
+    tail_slot = -1;
+    kept_entry = -1;
+    skip = 0;
+    if (pos < 0 || pos >= cap * G.bs || pos >= G.nb_max * G.bs) {
+      record_error(err, kErrCapacity, layer, r, pos);
+      skip = 1;
+    } else if (lcap > 0) {
+      const int32_t e = S.local_of[unit * G.nb_max + pos / G.bs];
+      if (e >= lcap) {
+        record_error(err, kErrLocalRange, layer, r, e);
+        skip = 1;
+      } else {
+        kept_entry = e;
+      }
     }
-    if (e >= 0)
-      kept = reinterpret_cast<T*>(T_.local_kv[r] + (((int64_t)layer * G.Hkv + h) * lcap + e) * G.block_bytes);
   }
-  T* summ = reinterpret_cast<T*>(S.summ) + (unit * G.nb_max + b) * 2 * G.d;
-  for (int32_t c = threadIdx.x; c < G.d; c += blockDim.x) {
-    const T k = k_new[unit * G.d + c];
-    const T v = v_new[unit * G.d + c];
-    host[kofs + c] = k;
-    host[vofs + c] = v;
-    if (pool) {
-      pool[kofs + c] = k;
-      pool[vofs + c] = v;
+  __syncthreads();
+  if (!skip) {
+    const int32_t b = pos / G.bs, t = pos % G.bs;
+    const int64_t kofs = (int64_t)t * G.d, vofs = (int64_t)(G.bs + t) * G.d;
+    for (int32_t s = threadIdx.x; s < G.kb; s += blockDim.x)
+      if (S.slot_block[unit * G.kb + s] == b) tail_slot = s;
+    __syncthreads();
+    T* host = reinterpret_cast<T*>(T_.host_kv[r] + (((int64_t)layer * G.Hkv + h) * cap + b) * G.block_bytes);
+    T* pool = tail_slot >= 0 ? reinterpret_cast<T*>(S.pool + (unit * G.kb + tail_slot) * G.block_bytes) : nullptr;
+    // a partially staged request also writes the decode side's kept copy of the block, if any
+    T* kept = kept_entry >= 0 ? reinterpret_cast<T*>(T_.local_kv[r] +
+                                                     (((int64_t)layer * G.Hkv + h) * lcap + kept_entry) *
+                                                         G.block_bytes)
+                              : nullptr;
+    T* summ = reinterpret_cast<T*>(S.summ) + (unit * G.nb_max + b) * 2 * G.d;
+    for (int32_t c = threadIdx.x; c < G.d; c += blockDim.x) {
+      const T k = k_new[unit * G.d + c];
+      const T v = v_new[unit * G.d + c];
+      host[kofs + c] = k;
+      host[vofs + c] = v;
+      if (pool) {
+        pool[kofs + c] = k;
+        pool[vofs + c] = v;
+      }
+      if (kept) {
+        kept[kofs + c] = k;
+        kept[vofs + c] = v;
+      }
+      if (t == 0) {
+        summ[c] = k;
+        summ[G.d + c] = k;
+      } else {
+        if (to_f(k) < to_f(summ[c])) summ[c] = k;
+        if (to_f(k) > to_f(summ[G.d + c])) summ[G.d + c] = k;
+      }
     }
-    if (kept) {
-      kept[kofs + c] = k;
-      kept[vofs + c] = v;
-    }
-    if (t == 0) {
-      summ[c] = k;
-      summ[G.d + c] = k;
-    } else {
-      if (to_f(k) < to_f(summ[c])) summ[c] = k;
-      if (to_f(k) > to_f(summ[G.d + c])) summ[G.d + c] = k;
-    }
+  }
+  // every CTA of the request has read the length before the last one advances it
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0 && atomicAdd(&arrivals[r], 1) == G.Hkv - 1) {
+    arrivals[r] = 0;
+    __threadfence();
+    S.len[r] = pos + 1;
   }
 }
 
@@ -161,11 +178,6 @@ __global__ void reset_request_kernel(Geom G, StateBase B, RequestInit q) {
   }
 }
 
-__global__ void advance_kernel(LayerState S, ReqTables T_, int32_t n_active) {
-  const int32_t i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < n_active) S.len[T_.active[i]] += 1;
-}
-
 }  // namespace
 
 cudaError_t launch_summary_build(const Geom& G, int32_t layer_begin, int32_t layer_end,
@@ -191,29 +203,23 @@ cudaError_t launch_summary_build(const Geom& G, int32_t layer_begin, int32_t lay
 }
 
 cudaError_t launch_append(const Geom& G, const LayerState& S, const ReqTables& T, int32_t n_active,
-                          int32_t layer, const void* k_new, const void* v_new, int32_t* err,
-                          cudaStream_t s) {
+                          int32_t layer, const void* k_new, const void* v_new, int32_t* arrivals,
+                          int32_t* err, cudaStream_t s) {
   if (n_active <= 0) return cudaSuccess;
   dim3 grid(n_active, G.Hkv);
   const int threads = G.d < 256 ? G.d : 256;
   if (G.dtype == OKV_F32)
     append_kernel<float><<<grid, threads, 0, s>>>(G, S, T, layer, (const float*)k_new,
-                                                  (const float*)v_new, err);
+                                                  (const float*)v_new, arrivals, err);
   else
     append_kernel<__nv_bfloat16><<<grid, threads, 0, s>>>(
-        G, S, T, layer, (const __nv_bfloat16*)k_new, (const __nv_bfloat16*)v_new, err);
+        G, S, T, layer, (const __nv_bfloat16*)k_new, (const __nv_bfloat16*)v_new, arrivals, err);
   return cudaGetLastError();
 }
 
 cudaError_t launch_reset_request(const Geom& G, const StateBase& B, const RequestInit& q, cudaStream_t s) {
   dim3 grid(G.L, G.Hkv);
   reset_request_kernel<<<grid, 256, 0, s>>>(G, B, q);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_advance(const LayerState& S, const ReqTables& T, int32_t n_active, cudaStream_t s) {
-  if (n_active <= 0) return cudaSuccess;
-  advance_kernel<<<(n_active + 127) / 128, 128, 0, s>>>(S, T, n_active);
   return cudaGetLastError();
 }
 

@@ -65,6 +65,11 @@ struct okv_ctx {
   uint32_t* scores = nullptr;    // [R][Hkv][nb_max]: block score images of the layer being staged
   int32_t* stage_arrivals = nullptr;   // [R * Hkv]: scoring CTAs finished per unit (kept at zero)
   int32_t* attend_arrivals = nullptr;  // [R * Hkv]: attention split CTAs finished per unit
+  int32_t* append_arrivals = nullptr;  // [layers][R]: append CTAs finished per request (kept at zero)
+  uint8_t* step_drafts = nullptr;      // [2][layers][R][Hq][d]: okv_step's copies of its drafts
+  int step_parity = 0;                 // which half of step_drafts the next okv_step fills
+  cudaEvent_t ev_step_read[2] = {nullptr, nullptr};  // the stagings of the last step using each half
+  bool step_used[2] = {false, false};
   bool stage_on_caller = false;  // run scoring/selection on the caller's stream (see okv_create)
   CUtensorMap pool_map;  // 64-byte aligned by its type
   bool have_map = false;
@@ -282,12 +287,14 @@ void okv_destroy(okv_ctx* c) {
   for (auto e : c->ev_selected) if (e) cudaEventDestroy(e);
   for (auto e : c->ev_staged) if (e) cudaEventDestroy(e);
   if (c->ev_in) cudaEventDestroy(c->ev_in);
+  for (auto e : c->ev_step_read) if (e) cudaEventDestroy(e);
   if (c->sel_stream) cudaStreamDestroy(c->sel_stream);
   if (c->copy_stream) cudaStreamDestroy(c->copy_stream);
   void* bufs[] = {c->summ, c->pool, c->slot_block, c->stamp, c->sel_ids, c->sel_scores,
                   c->n_sel, c->fetch, c->n_fetch, c->len, c->active_dev, c->host_kv_dev, c->cap_dev,
                   c->err_dev, c->ctr_dev, c->partials, c->draft_buf, c->scores, c->stage_arrivals, c->attend_arrivals,
-                  c->local_of, c->local_used, c->route, c->local_kv_dev, c->local_cap_dev};
+                  c->local_of, c->local_used, c->route, c->local_kv_dev, c->local_cap_dev,
+                  c->append_arrivals, c->step_drafts};
   for (void* p : bufs)
     if (p) cudaFree(p);
   delete c;
@@ -376,7 +383,8 @@ okv_status okv_create(const okv_config* cfg, okv_ctx** out) {
             alloc((void**)&c->stage_arrivals, (size_t)U * 4) && alloc((void**)&c->attend_arrivals, (size_t)U * 4) &&
             alloc((void**)&c->local_of, (size_t)L * U * G.nb_max * 4) && alloc((void**)&c->local_used, (size_t)L * U * 4) &&
             alloc((void**)&c->route, (size_t)L * U * G.kb * 4) && alloc((void**)&c->local_kv_dev, G.R * 8) &&
-            alloc((void**)&c->local_cap_dev, G.R * 4);
+            alloc((void**)&c->local_cap_dev, G.R * 4) && alloc((void**)&c->append_arrivals, (size_t)L * G.R * 4) &&
+            alloc((void**)&c->step_drafts, (size_t)2 * L * G.R * G.Hq * G.d * G.elem);
   if (ok) {
     size_t ws = 0;
     for (int32_t n = 1; n <= G.R; ++n) {
@@ -410,6 +418,7 @@ okv_status okv_create(const okv_config* cfg, okv_ctx** out) {
   ck(cudaMemset(c->route, 0xFF, (size_t)L * U * G.kb * 4));
   ck(cudaMemset(c->local_kv_dev, 0, G.R * 8));
   ck(cudaMemset(c->local_cap_dev, 0xFF, G.R * 4));
+  ck(cudaMemset(c->append_arrivals, 0, (size_t)L * G.R * 4));
   int lo = 0, hi = 0;
   ck(cudaDeviceGetStreamPriorityRange(&lo, &hi));
   // Scoring and selection run on the internal select stream at the least priority: they are
@@ -426,6 +435,7 @@ okv_status okv_create(const okv_config* cfg, okv_ctx** out) {
   ck(cudaStreamCreateWithPriority(&c->sel_stream, cudaStreamNonBlocking, prio));
   ck(cudaStreamCreateWithPriority(&c->copy_stream, cudaStreamNonBlocking, hi));
   ck(cudaEventCreateWithFlags(&c->ev_in, cudaEventDisableTiming));
+  for (auto& e : c->ev_step_read) ck(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
   c->ev_selected.assign(G.L, nullptr);
   c->ev_staged.assign(G.L, nullptr);
   c->staged_once.assign(G.L, 0);
@@ -656,16 +666,21 @@ okv_status okv_append(okv_ctx* c, int32_t layer, const void* k_new, const void* 
   const LayerState S = layer_state(c, layer);
   const ReqTables T = req_tables(c);
   Timer t(c, OKV_K_APPEND, s);
-  OKV_CUDA(c, okv::launch_append(G, S, T, n_active, layer, k_new, v_new, c->err_dev, s));
-  OKV_CUDA(c, okv::launch_advance(S, T, n_active, s));
-  t.stop(2);
+  OKV_CUDA(c, okv::launch_append(G, S, T, n_active, layer, k_new, v_new, c->append_arrivals + (size_t)layer * G.R,
+                                 c->err_dev, s));
+  t.stop(1);
   for (int32_t r : c->active_list) c->len_host[(size_t)layer * G.R + r] += 1;
   return OKV_OK;
 }
 
-okv_status okv_stage(okv_ctx* c, int32_t layer, const void* draft_q, int32_t step, float fetch_cap,
-                     void* stream) {
-  if (!c) return OKV_EINVAL;
+}  // extern "C"
+
+namespace {
+
+// `copied`: draft_q is already the library's own copy (okv_step copies every layer's draft at
+// once), so no per-layer copy is made and only the caller's work so far is waited for.
+okv_status stage_impl(okv_ctx* c, int32_t layer, const void* draft_q, bool copied, int32_t step, float fetch_cap,
+                      void* stream) {
   const Geom& G = c->G;
   if (layer < 0 || layer >= G.L) return fail(c, OKV_EINVAL, "okv_stage: layer %d out of range", layer);
   if (!draft_q) return fail(c, OKV_EINVAL, "okv_stage: NULL draft query");
@@ -679,7 +694,12 @@ okv_status okv_stage(okv_ctx* c, int32_t layer, const void* draft_q, int32_t ste
   const ReqTables T = req_tables(c);
   cudaStream_t ss = c->sel_stream;
   const void* draft_src = draft_q;
-  if (c->stage_on_caller) {
+  if (copied && !c->stage_on_caller) {
+    // scoring and selection follow the caller's work so far (its attention of this layer)
+    OKV_CUDA(c, cudaEventRecord(c->ev_in, s));
+    OKV_CUDA(c, cudaStreamWaitEvent(ss, c->ev_in, 0));
+    if (c->staged_once[layer]) OKV_CUDA(c, cudaStreamWaitEvent(ss, c->ev_staged[layer], 0));
+  } else if (c->stage_on_caller) {
     // scoring and selection follow the caller's attention of this layer on its own stream
     ss = s;
     if (c->staged_once[layer]) OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_staged[layer], 0));
@@ -713,6 +733,16 @@ okv_status okv_stage(okv_ctx* c, int32_t layer, const void* draft_q, int32_t ste
   OKV_CUDA(c, cudaEventRecord(c->ev_staged[layer], c->copy_stream));
   c->staged_once[layer] = 1;
   return OKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+okv_status okv_stage(okv_ctx* c, int32_t layer, const void* draft_q, int32_t step, float fetch_cap,
+                     void* stream) {
+  if (!c) return OKV_EINVAL;
+  return stage_impl(c, layer, draft_q, false, step, fetch_cap, stream);
 }
 
 namespace {
@@ -787,6 +817,19 @@ okv_status okv_step(okv_ctx* c, const void* q, const void* draft_q, void* out, c
   const Geom& G = c->G;
   const size_t qbytes = (size_t)G.R * G.Hq * G.d * G.elem;
   const size_t kvbytes = (size_t)G.R * G.Hkv * G.d * G.elem;
+  cudaStream_t s = (cudaStream_t)stream;
+  // One copy of every layer's draft, into the half of step_drafts the step before last used
+  // (its stagings have read it long since), instead of one copy per layer on the caller's stream.
+  const int p = c->step_parity;
+  const uint8_t* drafts = (const uint8_t*)draft_q;
+  const bool copied = !c->stage_on_caller;
+  if (copied) {
+    uint8_t* dst = c->step_drafts + (size_t)p * G.L * qbytes;
+    if (c->step_used[p]) OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_step_read[p], 0));
+    OKV_CUDA(c, cudaMemcpyAsync(dst, draft_q, (size_t)G.L * qbytes, cudaMemcpyDeviceToDevice, s));
+    drafts = dst;
+    c->step_parity ^= 1;
+  }
   for (int32_t l = 0; l < G.L; ++l) {
     if (k_new) {
       okv_status st = okv_append(c, l, (const uint8_t*)k_new + l * kvbytes, (const uint8_t*)v_new + l * kvbytes, stream);
@@ -794,8 +837,12 @@ okv_status okv_step(okv_ctx* c, const void* q, const void* draft_q, void* out, c
     }
     okv_status st = okv_attend(c, l, (const uint8_t*)q + l * qbytes, (uint8_t*)out + l * qbytes, stream);
     if (st != OKV_OK) return st;
-    st = okv_stage(c, l, (const uint8_t*)draft_q + l * qbytes, step, fetch_cap, stream);
+    st = stage_impl(c, l, drafts + l * qbytes, copied, step, fetch_cap, stream);
     if (st != OKV_OK) return st;
+  }
+  if (copied) {
+    OKV_CUDA(c, cudaEventRecord(c->ev_step_read[p], c->sel_stream));
+    c->step_used[p] = true;
   }
   return OKV_OK;
 }

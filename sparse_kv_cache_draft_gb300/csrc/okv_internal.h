@@ -74,9 +74,11 @@ cudaError_t launch_summary_build(const Geom& G, int32_t layer_begin, int32_t lay
                                  int32_t req, uint64_t host_kv, int32_t cap_blocks,
                                  int32_t n_tok, uint8_t* summ_base, int32_t* err,
                                  cudaStream_t s);
+// Append one token per active request at `layer` and advance the lengths; `arrivals`: [R] int32
+// that start at zero and are left at zero.
 cudaError_t launch_append(const Geom& G, const LayerState& S, const ReqTables& T, int32_t n_active,
-                          int32_t layer, const void* k_new, const void* v_new, int32_t* err,
-                          cudaStream_t s);
+                          int32_t layer, const void* k_new, const void* v_new, int32_t* arrivals,
+                          int32_t* err, cudaStream_t s);
 // Empties request `req`'s pool, tables and decode-side tier on every layer and records its
 // buffers (local_cap -1 and local_kv 0 for a request that holds its full KV).
 struct RequestInit {
@@ -89,7 +91,6 @@ struct StateBase {  // whole-context arrays, [layers] x per-layer block
   int32_t *cap_tab, *local_cap_tab;
 };
 cudaError_t launch_reset_request(const Geom& G, const StateBase& B, const RequestInit& q, cudaStream_t s);
-cudaError_t launch_advance(const LayerState& S, const ReqTables& T, int32_t n_active, cudaStream_t s);
 // Staging of one layer for every active unit: block scores (into `scores`, a [R][Hkv][nb_max]
 // uint32 workspace) by chunks of blocks; the last chunk of each unit to finish (counted in
 // `arrivals`, [R * Hkv] int32 that start at zero and are left at zero) runs the unit's top-K and
