@@ -171,10 +171,14 @@ OKV_API okv_status okv_attend_lookahead(okv_ctx* ctx, int32_t layer, const void*
 
 /* One decode step over every layer, in layer order ("4 System Design": the foreground waits
  * only for each layer's transfer; the background chain of layer l overlaps the attention of the
- * later layers): for l = 0 .. layers-1: okv_append(l) if k_new is not NULL, okv_attend(l),
- * okv_stage(l, step). q, draft_q, out: device [layers][max_requests][q_heads][head_dim];
- * k_new, v_new: device [layers][max_requests][kv_heads][head_dim] or NULL. Stops at the first
- * failing call and returns its status. */
+ * later layers). The result is that of: for l = 0 .. layers-1: okv_append(l) if k_new is not NULL,
+ * okv_attend(l), okv_stage(l, step). q, draft_q, out: device [layers][max_requests][q_heads]
+ * [head_dim]; k_new, v_new: device [layers][max_requests][kv_heads][head_dim] or NULL.
+ * Scheduling: every layer's draft is copied once, up front. Every layer's append is enqueued
+ * up front on an internal stream, each after that layer's previous staging. On `stream`, the
+ * attention of layer l waits only for the append of layer l. The inputs may be reused by work
+ * enqueued on `stream` after the call. Stops at the first failing check (before any work is
+ * enqueued, for the append checks) and returns its status. */
 OKV_API okv_status okv_step(okv_ctx* ctx, const void* q, const void* draft_q, void* out,
                             const void* k_new, const void* v_new, int32_t step, float fetch_cap,
                             void* stream);

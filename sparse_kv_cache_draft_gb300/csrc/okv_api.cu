@@ -86,6 +86,8 @@ struct okv_ctx {
 
   // streams and events
   cudaStream_t sel_stream = nullptr, copy_stream = nullptr;
+  cudaStream_t app_stream = nullptr;         // okv_step's appends, ahead of the caller's stream
+  std::vector<cudaEvent_t> ev_appended;      // [layers]: the last append of each layer
   cudaEvent_t ev_in = nullptr;
   std::vector<cudaEvent_t> ev_selected, ev_staged;
   std::vector<char> staged_once;
@@ -210,6 +212,7 @@ okv_status check_device_error(okv_ctx* c) {
 }
 
 okv_status sync_internal(okv_ctx* c) {
+  OKV_CUDA(c, cudaStreamSynchronize(c->app_stream));
   OKV_CUDA(c, cudaStreamSynchronize(c->sel_stream));
   OKV_CUDA(c, cudaStreamSynchronize(c->copy_stream));
   return OKV_OK;
@@ -279,6 +282,7 @@ void okv_destroy(okv_ctx* c) {
   if (!c) return;
   if (c->sel_stream) cudaStreamSynchronize(c->sel_stream);
   if (c->copy_stream) cudaStreamSynchronize(c->copy_stream);
+  if (c->app_stream) cudaStreamSynchronize(c->app_stream);
   for (auto& t : c->pending) {
     cudaEventDestroy(t.a);
     cudaEventDestroy(t.b);
@@ -286,10 +290,12 @@ void okv_destroy(okv_ctx* c) {
   for (auto e : c->event_pool) cudaEventDestroy(e);
   for (auto e : c->ev_selected) if (e) cudaEventDestroy(e);
   for (auto e : c->ev_staged) if (e) cudaEventDestroy(e);
+  for (auto e : c->ev_appended) if (e) cudaEventDestroy(e);
   if (c->ev_in) cudaEventDestroy(c->ev_in);
   for (auto e : c->ev_step_read) if (e) cudaEventDestroy(e);
   if (c->sel_stream) cudaStreamDestroy(c->sel_stream);
   if (c->copy_stream) cudaStreamDestroy(c->copy_stream);
+  if (c->app_stream) cudaStreamDestroy(c->app_stream);
   void* bufs[] = {c->summ, c->pool, c->slot_block, c->stamp, c->sel_ids, c->sel_scores,
                   c->n_sel, c->fetch, c->n_fetch, c->len, c->active_dev, c->host_kv_dev, c->cap_dev,
                   c->err_dev, c->ctr_dev, c->partials, c->draft_buf, c->scores, c->stage_arrivals, c->attend_arrivals,
@@ -434,14 +440,17 @@ okv_status okv_create(const okv_config* cfg, okv_ctx** out) {
   c->stage_on_caller = ps && strcmp(ps, "caller") == 0;
   ck(cudaStreamCreateWithPriority(&c->sel_stream, cudaStreamNonBlocking, prio));
   ck(cudaStreamCreateWithPriority(&c->copy_stream, cudaStreamNonBlocking, hi));
+  ck(cudaStreamCreateWithPriority(&c->app_stream, cudaStreamNonBlocking, hi));
   ck(cudaEventCreateWithFlags(&c->ev_in, cudaEventDisableTiming));
   for (auto& e : c->ev_step_read) ck(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
   c->ev_selected.assign(G.L, nullptr);
   c->ev_staged.assign(G.L, nullptr);
+  c->ev_appended.assign(G.L, nullptr);
   c->staged_once.assign(G.L, 0);
   for (int32_t l = 0; l < G.L; ++l) {
     ck(cudaEventCreateWithFlags(&c->ev_selected[l], cudaEventDisableTiming));
     ck(cudaEventCreateWithFlags(&c->ev_staged[l], cudaEventDisableTiming));
+    ck(cudaEventCreateWithFlags(&c->ev_appended[l], cudaEventDisableTiming));
   }
   c->active.assign(G.R, 0);
   c->host_ptr.assign(G.R, nullptr);
@@ -647,11 +656,13 @@ okv_status okv_remove_request(okv_ctx* c, int32_t req) {
   return upload_active(c);
 }
 
-okv_status okv_append(okv_ctx* c, int32_t layer, const void* k_new, const void* v_new, void* stream) {
-  if (!c) return OKV_EINVAL;
+}  // extern "C"
+
+namespace {
+
+okv_status append_check(okv_ctx* c, int32_t layer) {
   const Geom& G = c->G;
   if (layer < 0 || layer >= G.L) return fail(c, OKV_EINVAL, "okv_append: layer %d out of range", layer);
-  if (!k_new || !v_new) return fail(c, OKV_EINVAL, "okv_append: NULL input");
   for (int32_t r : c->active_list) {
     if (c->shared_buf[r])
       return fail(c, OKV_EINVAL, "okv_append: request %d shares its host buffer with another active request", r);
@@ -659,9 +670,15 @@ okv_status okv_append(okv_ctx* c, int32_t layer, const void* k_new, const void* 
     if ((int64_t)n >= (int64_t)c->cap_blocks[r] * G.bs)
       return fail(c, OKV_EINVAL, "okv_append: request %d is full at layer %d", r, layer);
   }
+  return OKV_OK;
+}
+
+// Enqueue the append of one layer on `s`, after the layer's last staging (its gather may have
+// written the tail block's slot and read the host block the append writes).
+okv_status append_enqueue(okv_ctx* c, int32_t layer, const void* k_new, const void* v_new, cudaStream_t s) {
+  const Geom& G = c->G;
   const int32_t n_active = (int32_t)c->active_list.size();
   if (n_active == 0) return OKV_OK;
-  cudaStream_t s = (cudaStream_t)stream;
   if (c->staged_once[layer]) OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_staged[layer], 0));
   const LayerState S = layer_state(c, layer);
   const ReqTables T = req_tables(c);
@@ -671,6 +688,17 @@ okv_status okv_append(okv_ctx* c, int32_t layer, const void* k_new, const void* 
   t.stop(1);
   for (int32_t r : c->active_list) c->len_host[(size_t)layer * G.R + r] += 1;
   return OKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+okv_status okv_append(okv_ctx* c, int32_t layer, const void* k_new, const void* v_new, void* stream) {
+  if (!c) return OKV_EINVAL;
+  if (!k_new || !v_new) return fail(c, OKV_EINVAL, "okv_append: NULL input");
+  if (okv_status st = append_check(c, layer)) return st;
+  return append_enqueue(c, layer, k_new, v_new, (cudaStream_t)stream);
 }
 
 }  // extern "C"
@@ -830,11 +858,22 @@ okv_status okv_step(okv_ctx* c, const void* q, const void* draft_q, void* out, c
     drafts = dst;
     c->step_parity ^= 1;
   }
-  for (int32_t l = 0; l < G.L; ++l) {
-    if (k_new) {
-      okv_status st = okv_append(c, l, (const uint8_t*)k_new + l * kvbytes, (const uint8_t*)v_new + l * kvbytes, stream);
+  if (k_new) {
+    // Every layer's append goes on the append stream at once, each after its layer's last
+    // staging; the caller's stream waits for a layer's append only before that layer's attention.
+    for (int32_t l = 0; l < G.L; ++l)
+      if (okv_status st = append_check(c, l)) return st;
+    OKV_CUDA(c, cudaEventRecord(c->ev_in, s));  // k_new / v_new are ready
+    OKV_CUDA(c, cudaStreamWaitEvent(c->app_stream, c->ev_in, 0));
+    for (int32_t l = 0; l < G.L; ++l) {
+      okv_status st = append_enqueue(c, l, (const uint8_t*)k_new + l * kvbytes, (const uint8_t*)v_new + l * kvbytes,
+                                     c->app_stream);
       if (st != OKV_OK) return st;
+      OKV_CUDA(c, cudaEventRecord(c->ev_appended[l], c->app_stream));
     }
+  }
+  for (int32_t l = 0; l < G.L; ++l) {
+    if (k_new) OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_appended[l], 0));
     okv_status st = okv_attend(c, l, (const uint8_t*)q + l * qbytes, (uint8_t*)out + l * qbytes, stream);
     if (st != OKV_OK) return st;
     st = stage_impl(c, l, drafts + l * qbytes, copied, step, fetch_cap, stream);
@@ -850,6 +889,8 @@ okv_status okv_step(okv_ctx* c, const void* q, const void* draft_q, void* out, c
 okv_status okv_join(okv_ctx* c, void* stream) {
   if (!c) return OKV_EINVAL;
   cudaStream_t s = (cudaStream_t)stream;
+  OKV_CUDA(c, cudaEventRecord(c->ev_in, c->app_stream));
+  OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_in, 0));
   OKV_CUDA(c, cudaEventRecord(c->ev_in, c->sel_stream));
   OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_in, 0));
   OKV_CUDA(c, cudaEventRecord(c->ev_in, c->copy_stream));
