@@ -900,20 +900,28 @@ okv_status okv_join(okv_ctx* c, void* stream) {
 
 okv_status okv_sync(okv_ctx* c, int64_t timeout_ms) {
   if (!c) return OKV_EINVAL;
-  cudaEvent_t ea = nullptr, eb = nullptr;
-  OKV_CUDA(c, cudaEventCreateWithFlags(&ea, cudaEventDisableTiming));
-  OKV_CUDA(c, cudaEventCreateWithFlags(&eb, cudaEventDisableTiming));
-  OKV_CUDA(c, cudaEventRecord(ea, c->sel_stream));
-  OKV_CUDA(c, cudaEventRecord(eb, c->copy_stream));
+  // one event at the end of each internal stream (staging, gather, appends of okv_step)
+  cudaStream_t streams[3] = {c->sel_stream, c->copy_stream, c->app_stream};
+  cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
+  for (int i = 0; i < 3; ++i) {
+    OKV_CUDA(c, cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming));
+    OKV_CUDA(c, cudaEventRecord(ev[i], streams[i]));
+  }
   const auto t0 = std::chrono::steady_clock::now();
   okv_status st = OKV_OK;
   for (;;) {
-    const cudaError_t qa = cudaEventQuery(ea), qb = cudaEventQuery(eb);
-    if (qa == cudaSuccess && qb == cudaSuccess) break;
-    if ((qa != cudaSuccess && qa != cudaErrorNotReady) || (qb != cudaSuccess && qb != cudaErrorNotReady)) {
-      st = fail(c, OKV_ECUDA, "okv_sync: %s", cudaGetErrorString(qa != cudaSuccess && qa != cudaErrorNotReady ? qa : qb));
+    bool done = true;
+    cudaError_t bad = cudaSuccess;
+    for (int i = 0; i < 3; ++i) {
+      const cudaError_t q = cudaEventQuery(ev[i]);
+      if (q == cudaErrorNotReady) done = false;
+      else if (q != cudaSuccess) bad = q;
+    }
+    if (bad != cudaSuccess) {
+      st = fail(c, OKV_ECUDA, "okv_sync: %s", cudaGetErrorString(bad));
       break;
     }
+    if (done) break;
     const auto ms = std::chrono::duration_cast<std::chrono::milliseconds>(std::chrono::steady_clock::now() - t0).count();
     if (timeout_ms >= 0 && ms > timeout_ms) {
       st = fail(c, OKV_ETIMEOUT, "okv_sync: work still running after %lld ms", (long long)timeout_ms);
@@ -921,8 +929,7 @@ okv_status okv_sync(okv_ctx* c, int64_t timeout_ms) {
     }
     std::this_thread::sleep_for(std::chrono::microseconds(50));
   }
-  cudaEventDestroy(ea);
-  cudaEventDestroy(eb);
+  for (auto e : ev) cudaEventDestroy(e);
   if (st != OKV_OK) return st;
   return check_device_error(c);
 }

@@ -284,3 +284,53 @@ def test_sync_deadline_reports_timeout():
         rig.check_tables(0)
     finally:
         rig.close()
+
+
+def test_step_with_appends_every_unit():
+    """okv_step with appends (every layer's append on the library's own stream, each after its
+    layer's previous staging) over 20 steps across block boundaries, 3 layers x 3 requests:
+    attention, selections, tables and pools of every unit after every step."""
+    import torch
+    import oracle as O
+    from okv_harness import to_device, torch_dtype
+    w = QWEN.scaled(layers=3, batch=3, steps=20)
+    rig = Rig(w, contexts=[1000, 2040, 3000], capacity_tokens=3100)
+    try:
+        L, R, Hq, Hkv, d = w.layers, rig.R, w.q_heads, w.kv_heads, w.head_dim
+        C = O.fetch_cap_blocks(w.fetch_cap, rig.kb)
+
+        def all_layers(step, kind):
+            return np.stack([rig.batch_queries(l, step, kind) for l in range(L)])
+
+        d_boot = all_layers(-1, 1)
+        for l in range(L):
+            rig.ctx.stage(l, to_device(d_boot[l], w.dtype), 0, 1.0)
+        torch.cuda.synchronize()
+        for l in range(L):
+            rig._ensure_summaries(l)
+            rig.model.score_topk(l, d_boot[l])
+            gsel, _ = rig.check_selection(l)
+            rig.model.select(l, O.fetch_cap_blocks(1.0, rig.kb), 0, sel_override=gsel)
+        for t in range(w.steps):
+            kv = [synth.token_kv(w, l, rig.keys, rig.model.n_tok[l], plant_blocks=rig.plant_blocks) for l in range(L)]
+            k_all = np.stack([k for k, _ in kv])
+            v_all = np.stack([v for _, v in kv])
+            q, dr = all_layers(t, 0), all_layers(t, 1)
+            out = torch.zeros((L, R, Hq, d), dtype=torch_dtype(w.dtype), device="cuda")
+            rig.ctx.step(to_device(q, w.dtype), to_device(dr, w.dtype), out, t + 1,
+                         k_new=to_device(k_all, w.dtype), v_new=to_device(v_all, w.dtype))
+            torch.cuda.synchronize()
+            assert rig.ctx.sync(60_000) == 0
+            for l in range(L):
+                rig.model.append(l, k_all[l], v_all[l])
+                assert rig.check_attention(l, q[l], out[l]) <= ATOL[BF16]
+                rig.model.score_topk(l, dr[l])
+                gsel, _ = rig.check_selection(l)
+                rig.model.select(l, C, t + 1, sel_override=gsel)
+                rig.check_tables(l)
+                rig.check_pool(l)
+        for l in range(L):
+            rig.check_summaries(l)
+            assert rig.ctx.read_lengths(l)[:3].tolist() == [1020, 2060, 3020]
+    finally:
+        rig.close()
