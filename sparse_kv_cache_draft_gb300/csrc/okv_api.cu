@@ -5,12 +5,13 @@
 // background chain of top-K prediction, KV selection and KV transfer runs on independent
 // workers overlapped across layers and steps; the foreground waits only for that layer's
 // transfer):
-//   caller stream : [wait staged(l)] attend(l)            [wait staged(l)] append(l)
+//   caller stream : [wait staged(l)] attend(l)      (okv_append: [wait staged(l)] append(l))
 //   select stream : [wait caller] [wait staged(l)] score+top-K(l) -> select(l) -> selected(l)
 //   copy stream   : [wait selected(l)] gather(l) -> staged(l)
+//   append stream : okv_step's appends, all enqueued up front: [wait staged(l)] append(l) -> appended(l)
 // Staging of layer l at step t starts after the work the caller enqueued before it (its
 // attention of layer l at step t, which reads the slots the gather may overwrite), and the
-// attention of layer l at step t+1 waits only for staged(l).
+// attention of layer l at step t+1 waits only for staged(l) (and, in okv_step, appended(l)).
 #include <math.h>
 #include <stdarg.h>
 #include <stdio.h>
