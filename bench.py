@@ -938,6 +938,7 @@ def run_append(args, dist: Dist):
             "step_hbm_gbs": round((att_bytes + summ_bytes) / (step_ms / 1e3) / 1e9, 1),
             "step_hbm_frac": round((att_bytes + summ_bytes) / (step_ms / 1e3) / 1e9 / hbm_peak, 4),
             "gather_gb_per_step": round(tm["fetched_blocks"] * slot_bytes / K / 1e9, 4),
+            "kernel_ms_per_step": {k: round(v / K, 4) for k, v in tm["ms"].items() if v > 0},
             "peak_source": f"hbm_gbs, {src}"}
 
 
