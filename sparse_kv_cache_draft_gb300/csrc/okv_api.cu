@@ -428,12 +428,15 @@ okv_status okv_create(const okv_config* cfg, okv_ctx** out) {
   ck(cudaMemset(c->append_arrivals, 0, (size_t)L * G.R * 4));
   int lo = 0, hi = 0;
   ck(cudaDeviceGetStreamPriorityRange(&lo, &hi));
-  // Scoring and selection run on the internal select stream at the least priority: they are
-  // bound by HBM bandwidth like the attention, so they only fill the SMs the attention leaves
-  // idle. The gather runs on the copy stream at the greatest priority: the host link is the
-  // longest pole of a step, so it must never wait for SMs. (Measured on GB300, 16K / b128:
-  // 10.2K tok/s, against 9.4K with scoring on the caller's stream after the attention and 8.2K
-  // with scoring at the greatest priority.) OKV_STAGE_STREAM=caller and OKV_STAGE_PRIORITY=high
+  // Scoring and selection run on the internal select stream at the least priority, which is
+  // also the priority of the default streams a caller's attention usually runs on: the two
+  // HBM-bound kernels share the SMs as equals. (Measured on GB300, 16K / b128: 10.2K tok/s
+  // against 9.4K with scoring on the caller's stream after the attention and 8.2K with staging
+  // at the greatest priority; running okv_step's attentions on a
+  // stream above the staging raised the attention's in-step share of the HBM peak from 0.64 to
+  // 0.73 but cost 4% of tok/s, the staging then falling behind the gather.) The gather runs on
+  // the copy stream at the greatest priority: the host link is the longest pole of a step, so
+  // the gather must never wait for SMs. OKV_STAGE_STREAM=caller and OKV_STAGE_PRIORITY=high
   // select the alternatives.
   const char* pe = getenv("OKV_STAGE_PRIORITY");
   const int prio = (pe && strcmp(pe, "high") == 0) ? hi : lo;  // of the select stream
