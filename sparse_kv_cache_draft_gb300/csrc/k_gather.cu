@@ -11,6 +11,7 @@
 // from the decode side's kept copy when it has one; a block fetched for the first time comes
 // from the full copy and is also written to the decode-side entry the selection assigned.
 #include <stdlib.h>
+#include <string.h>
 
 #include "okv_internal.h"
 
@@ -28,17 +29,27 @@ __device__ __forceinline__ void record_error(int32_t* err, int32_t code, int32_t
   }
 }
 
-// Persistent grid: warp w of the grid copies work items w, w + nwarps, ... where item i is
-// entry i % cmax of active unit i / cmax (items past the unit's fetch count are skipped).
+// Persistent grid over work items, item i being entry i % cmax of active unit i / cmax (items
+// past the unit's fetch count are skipped). With `work` set, warps claim items one at a time
+// from work[0], so they finish together instead of at the end of fixed shares whose host-read
+// latencies differ; the last CTA to leave (counted in work[1]) resets both counters. Without
+// it, warp w copies items w, w + nwarps, ...
 template <int kVecPerLane>
 __global__ void __launch_bounds__(kGatherWarps * 32)
 gather_kernel(Geom G, LayerState S, ReqTables RT, int32_t layer, int32_t n_units, int32_t cmax,
-              int32_t* err) {
+              int32_t* work, int32_t* err) {
   const int lane = threadIdx.x & 31;
   const int64_t nw = (int64_t)gridDim.x * kGatherWarps;
   const int64_t total = (int64_t)n_units * cmax;
   const int32_t nvec = (int32_t)(G.block_bytes / 16);
-  for (int64_t it = (int64_t)blockIdx.x * kGatherWarps + (threadIdx.x >> 5); it < total; it += nw) {
+  int64_t it = (int64_t)blockIdx.x * kGatherWarps + (threadIdx.x >> 5);
+  for (;; it += nw) {
+    if (work) {
+      int32_t claimed = 0;
+      if (lane == 0) claimed = atomicAdd(&work[0], 1);
+      it = __shfl_sync(0xffffffffu, claimed, 0);
+    }
+    if (it >= total) break;
     const int32_t ua = (int32_t)(it / cmax), e = (int32_t)(it % cmax);
     const int32_t a = ua / G.Hkv, h = ua % G.Hkv;
     const int32_t r = RT.active[a];
@@ -95,12 +106,19 @@ gather_kernel(Geom G, LayerState S, ReqTables RT, int32_t layer, int32_t n_units
       }
     }
   }
+  if (work) {
+    __syncthreads();
+    if (threadIdx.x == 0 && atomicAdd(&work[1], 1) == (int32_t)gridDim.x - 1) {
+      work[0] = 0;
+      work[1] = 0;
+    }
+  }
 }
 
 }  // namespace
 
 cudaError_t launch_gather(const Geom& G, const LayerState& S, const ReqTables& T, int32_t n_active,
-                          int32_t layer, int32_t max_fetch, int32_t* err, cudaStream_t s) {
+                          int32_t layer, int32_t max_fetch, int32_t* work, int32_t* err, cudaStream_t s) {
   if (n_active <= 0 || max_fetch <= 0) return cudaSuccess;
   // A few warps keep enough host reads in flight to fill the host link; more of them only slow
   // the HBM-bound kernels running beside the gather (measured on GB300: 32 CTAs of 4 warps move
@@ -113,7 +131,12 @@ cudaError_t launch_gather(const Geom& G, const LayerState& S, const ReqTables& T
   const int64_t items = (int64_t)n_active * G.Hkv * max_fetch;
   const int64_t want = (items + kGatherWarps - 1) / kGatherWarps;
   const int grid = (int)(want < ctas ? want : ctas);
-  gather_kernel<16><<<grid, kGatherWarps * 32, 0, s>>>(G, S, T, layer, n_active * G.Hkv, max_fetch, err);
+  static const bool dynamic = [] {
+    const char* e = getenv("OKV_GATHER_DYNAMIC");
+    return !(e && strcmp(e, "0") == 0);
+  }();
+  gather_kernel<16><<<grid, kGatherWarps * 32, 0, s>>>(G, S, T, layer, n_active * G.Hkv, max_fetch,
+                                                       dynamic ? work : nullptr, err);
   return cudaGetLastError();
 }
 

@@ -67,6 +67,7 @@ struct okv_ctx {
   int32_t* stage_arrivals = nullptr;   // [R * Hkv]: scoring CTAs finished per unit (kept at zero)
   int32_t* attend_arrivals = nullptr;  // [R * Hkv]: attention split CTAs finished per unit
   int32_t* append_arrivals = nullptr;  // [layers][R]: append CTAs finished per request (kept at zero)
+  int32_t* gather_work = nullptr;      // [layers][2]: gather work and exit counters (kept at zero)
   uint8_t* step_drafts = nullptr;      // [2][layers][R][Hq][d]: okv_step's copies of its drafts
   int step_parity = 0;                 // which half of step_drafts the next okv_step fills
   cudaEvent_t ev_step_read[2] = {nullptr, nullptr};  // the stagings of the last step using each half
@@ -301,7 +302,7 @@ void okv_destroy(okv_ctx* c) {
                   c->n_sel, c->fetch, c->n_fetch, c->len, c->active_dev, c->host_kv_dev, c->cap_dev,
                   c->err_dev, c->ctr_dev, c->partials, c->draft_buf, c->scores, c->stage_arrivals, c->attend_arrivals,
                   c->local_of, c->local_used, c->route, c->local_kv_dev, c->local_cap_dev,
-                  c->append_arrivals, c->step_drafts};
+                  c->append_arrivals, c->step_drafts, c->gather_work};
   for (void* p : bufs)
     if (p) cudaFree(p);
   delete c;
@@ -391,7 +392,8 @@ okv_status okv_create(const okv_config* cfg, okv_ctx** out) {
             alloc((void**)&c->local_of, (size_t)L * U * G.nb_max * 4) && alloc((void**)&c->local_used, (size_t)L * U * 4) &&
             alloc((void**)&c->route, (size_t)L * U * G.kb * 4) && alloc((void**)&c->local_kv_dev, G.R * 8) &&
             alloc((void**)&c->local_cap_dev, G.R * 4) && alloc((void**)&c->append_arrivals, (size_t)L * G.R * 4) &&
-            alloc((void**)&c->step_drafts, (size_t)2 * L * G.R * G.Hq * G.d * G.elem);
+            alloc((void**)&c->step_drafts, (size_t)2 * L * G.R * G.Hq * G.d * G.elem) &&
+            alloc((void**)&c->gather_work, (size_t)L * 2 * 4);
   if (ok) {
     size_t ws = 0;
     for (int32_t n = 1; n <= G.R; ++n) {
@@ -426,6 +428,7 @@ okv_status okv_create(const okv_config* cfg, okv_ctx** out) {
   ck(cudaMemset(c->local_kv_dev, 0, G.R * 8));
   ck(cudaMemset(c->local_cap_dev, 0xFF, G.R * 4));
   ck(cudaMemset(c->append_arrivals, 0, (size_t)L * G.R * 4));
+  ck(cudaMemset(c->gather_work, 0, (size_t)L * 2 * 4));
   int lo = 0, hi = 0;
   ck(cudaDeviceGetStreamPriorityRange(&lo, &hi));
   // Scoring and selection run on the internal select stream at the least priority, which is
@@ -759,7 +762,8 @@ okv_status stage_impl(okv_ctx* c, int32_t layer, const void* draft_q, bool copie
   OKV_CUDA(c, cudaStreamWaitEvent(c->copy_stream, c->ev_selected[layer], 0));
   {
     Timer t(c, OKV_K_GATHER, c->copy_stream);
-    OKV_CUDA(c, okv::launch_gather(G, S, T, n_active, layer, C, c->err_dev, c->copy_stream));
+    OKV_CUDA(c, okv::launch_gather(G, S, T, n_active, layer, C, c->gather_work + 2 * layer, c->err_dev,
+                                   c->copy_stream));
     t.stop(1);
   }
   OKV_CUDA(c, cudaEventRecord(c->ev_staged[layer], c->copy_stream));

@@ -103,8 +103,9 @@ cudaError_t launch_stage(const Geom& G, const LayerState& S, const ReqTables& T,
                          int32_t max_nb, const void* draft, uint32_t* scores, int32_t* arrivals,
                          int32_t cap_blocks, int32_t step, Counters* ctr, int32_t* err, cudaStream_t s,
                          int* n_launches, int32_t* pred_ids = nullptr, int32_t* pred_n = nullptr);
+// `work`: two int32 counters of this layer that start at zero and are left at zero.
 cudaError_t launch_gather(const Geom& G, const LayerState& S, const ReqTables& T, int32_t n_active,
-                          int32_t layer, int32_t max_fetch, int32_t* err, cudaStream_t s);
+                          int32_t layer, int32_t max_fetch, int32_t* work, int32_t* err, cudaStream_t s);
 // Attention: decides between the tensor-core path (bf16, d = 128, g <= 8) and the CUDA-core
 // path; `partials` is a workspace of at least attend_workspace_bytes() bytes.
 size_t attend_workspace_bytes(const Geom& G, int32_t n_active);
