@@ -57,3 +57,24 @@ def test_ranks_share_the_host():
     assert bench.rank_host_share(16, 0, 16)[0] == 2
     assert bench.rank_host_share(16, 3, 4) == (4, 3)
     assert bench.rank_host_share(16, 0, 4)[1] >= 1
+
+
+def test_profiled_traffic_follows_the_kernel_sources(tmp_path, monkeypatch):
+    """bench.py reports an ncu traffic figure only while the sources it names still hash as
+    recorded (a changed kernel makes the figure null)."""
+    import hashlib
+    import bench
+    (tmp_path / "profiles").mkdir()
+    srcs = ["a.cu", "b.h"]
+    for n, text in zip(srcs, ("kernel v1\n", "header\n")):
+        (tmp_path / n).write_text(text)
+    h = hashlib.sha256()
+    for n in srcs:
+        h.update((tmp_path / n).read_bytes())
+    (tmp_path / "profiles" / "k.md").write_text(
+        f"notes\n    bench: traffic_bytes_per_launch=12345 source={','.join(srcs)} sha256_16={h.hexdigest()[:16]}\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.profiled_traffic("k.md") == 12345
+    (tmp_path / "b.h").write_text("header, changed\n")
+    assert bench.profiled_traffic("k.md") is None
+    assert bench.profiled_traffic("missing.md") is None
