@@ -266,12 +266,19 @@ OKV_API int64_t okv_launch_count(const okv_ctx* ctx);
  * Limits: n_requests <= 16384, and the split workspace the launch shape needs must fit in the
  * array (about 16 MiB of n_requests * kv_heads * split * g * (head_dim + 2) floats); beyond
  * them, and for shapes okv_create refuses, the call returns OKV_EINVAL without launching.
- * The first call on a device resolves the array's device address (cudaGetSymbolAddress) and
- * initialises its constant part, synchronising that device: make it before any stream
- * capture. Later calls only enqueue on `stream`. All calls share the array: calls whose work
- * overlaps on the GPU (on different streams, or on different host threads) race and must be
- * serialised by the caller. Indices that fail the kernels' bounds checks are skipped; this
- * call has no context to report them through. */
+ * Every call resolves the array's device address on the current device
+ * (cudaGetSymbolAddress). The first call in each CUDA context of a device (the first call on
+ * the device, and the first after a cudaDeviceReset) also initialises the array's constant
+ * part, synchronising that device: make it before any stream capture. Calls then enqueue on
+ * `stream`, which must belong to the current device (else OKV_EINVAL): two small clears of
+ * the array (split counters, error word), then the attention kernels. All calls share the
+ * array: calls whose work overlaps on the GPU (on different streams, or on different host
+ * threads) race and must be serialised by the caller.
+ * Failures the kernels record are not reported: this call has no context to report them
+ * through. A slot whose block id fails the bounds check (outside the request's length) is
+ * skipped, and a copy wait that gives up leaves the unit's output partial; the array's error
+ * word holds the first such failure of the call until the next call clears it, and no call
+ * reads it. */
 OKV_API okv_status okv_attend_static(int32_t n_requests, int32_t q_heads, int32_t kv_heads,
                                      int32_t head_dim, int32_t block_size, int32_t slots,
                                      int32_t dtype, const void* pool, const int32_t* slot_block,

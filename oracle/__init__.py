@@ -205,9 +205,18 @@ def append(host_unit: np.ndarray, summ: np.ndarray, n_tok: int, bs: int, d: int,
 class OracleModel:
     """The oracle's copy of the staging state for every (layer, request, kv head).
 
-    Host KV is read through raw addresses: ``req_ptrs[r]`` is request r's buffer, laid out
-    [layers][kv_heads][cap_blocks[r]][2][bs][d] in the storage type (the same bytes the GPU
-    library reads). Summaries and the per-unit tables live in numpy arrays here.
+    Host KV comes in one of two ways:
+
+    * ``host_fill`` (what the parity tests use): the oracle keeps a private copy of every kept
+      layer of every distinct content, ``req_keys[r]`` naming request r's content. The copy of
+      (layer, key) is a [kv_heads][cap_blocks][2][bs][d] array of the storage type that
+      ``host_fill(layer, key, array)`` fills from the seeded generator. Requests with the same
+      key share it. Nothing the CUDA library writes reaches these bytes: appends are applied
+      to them by :meth:`append`.
+    * ``req_ptrs`` (timing only): request r's buffer at a raw address, laid out
+      [layers][kv_heads][cap_blocks[r]][2][bs][d].
+
+    Summaries and the per-unit tables live in numpy arrays here.
 
     ``local_cap[r]`` >= 0 marks request r as partially staged: its fetch lists are also routed
     through a decode-side tier of that many entries per unit (``local_of``, ``local_used``,
@@ -215,16 +224,18 @@ class OracleModel:
     """
 
     def __init__(self, *, layers, q_heads, kv_heads, head_dim, block_size, budget_tokens,
-                 dtype, req_ptrs, cap_blocks, n_tok, n_threads=None, layers_kept=None,
-                 local_cap=None):
+                 dtype, cap_blocks, n_tok, req_ptrs=None, host_fill=None, req_keys=None,
+                 n_threads=None, layers_kept=None, local_cap=None):
         self.L, self.Hq, self.Hkv, self.d, self.bs = layers, q_heads, kv_heads, head_dim, block_size
         self.g = q_heads // kv_heads
         self.kb = budget_tokens // block_size
         self.dtype = dtype
         self.elem = 4 if dtype == F32 else 2
         self.sdt = np.float32 if dtype == F32 else np.uint16
-        self.B = len(req_ptrs)
-        self.req_ptrs = [int(p) for p in req_ptrs]
+        if (req_ptrs is None) == (host_fill is None):
+            raise ValueError("give either req_ptrs or host_fill")
+        self.B = len(req_ptrs) if req_ptrs is not None else len(req_keys)
+        self.req_ptrs = [int(p) for p in req_ptrs] if req_ptrs is not None else None
         self.cap_blocks = np.asarray(cap_blocks, dtype=np.int64)
         self.n_tok = np.array(np.broadcast_to(np.asarray(n_tok, dtype=np.int32),
                                               (layers, self.B)))
@@ -247,13 +258,28 @@ class OracleModel:
         self.local_of = {l: np.full(shp + (self.nb_max,), -1, dtype=np.int32) for l in self.layers_kept}
         self.local_used = {l: np.zeros(shp, dtype=np.int32) for l in self.layers_kept}
         self.route = {l: np.full(shp + (self.kb,), -1, dtype=np.int32) for l in self.layers_kept}
+        self.host = None
+        if host_fill is not None:
+            self.req_keys = [int(k) for k in req_keys]
+            self.host = {}
+            for l in self.layers_kept:
+                for r, k in enumerate(self.req_keys):
+                    if (l, k) in self.host:
+                        continue
+                    a = np.zeros((self.Hkv, int(self.cap_blocks[r]), 2, self.bs, self.d), dtype=self.sdt)
+                    host_fill(l, k, a)
+                    self.host[(l, k)] = a
 
     def host_unit_ptr(self, layer: int, r: int, h: int) -> int:
+        if self.host is not None:
+            return self.host[(layer, self.req_keys[r])][h].ctypes.data
         unit = int(self.cap_blocks[r]) * 2 * self.bs * self.d
         return self.req_ptrs[r] + (layer * self.Hkv + h) * unit * self.elem
 
     def host_unit(self, layer: int, r: int, h: int) -> np.ndarray:
-        """numpy view of one unit's host region (no copy)."""
+        """numpy view of one unit's host region (no copy): [cap_blocks][2][bs][d]."""
+        if self.host is not None:
+            return self.host[(layer, self.req_keys[r])][h]
         n = int(self.cap_blocks[r]) * 2 * self.bs * self.d
         buf = (ctypes.c_char * (n * self.elem)).from_address(self.host_unit_ptr(layer, r, h))
         return np.frombuffer(buf, dtype=self.sdt).reshape(int(self.cap_blocks[r]), 2, self.bs, self.d)

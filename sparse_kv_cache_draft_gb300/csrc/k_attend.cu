@@ -78,11 +78,13 @@ __device__ int32_t build_items(const Geom& G, const int32_t* slot_block, int32_t
     if (s < s_hi) {
       const int32_t b = slot_block[s];
       if (b >= 0) {
-        const int32_t nv = min(G.bs, len - b * G.bs);
-        if (nv <= 0 || b >= G.nb_max)
+        // tokens of block b within the context, in 64 bits: b * bs may pass 2^31 for a block id
+        // that fails the check
+        const int64_t rem = (int64_t)len - (int64_t)b * G.bs;
+        if (rem <= 0 || b >= G.nb_max)
           record_error(err, kErrBlockRange, -2, r, b);
         else
-          item = (s << 8) | nv;
+          item = (s << 8) | (int32_t)(rem < G.bs ? rem : G.bs);
       }
     }
     const unsigned ballot = __ballot_sync(0xffffffffu, item >= 0);
@@ -668,21 +670,45 @@ __global__ void static_init_kernel(int32_t* ids, int32_t n, int32_t* err, okv::C
   }
 }
 
-std::mutex g_static_mu;
-void* g_static_base[256] = {};  // device address of okv_static_scratch, per device ordinal
+void* driver_entry(const char* name) {
+  void* f = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return f;
+}
 
-// Once per device, with that device current: resolve the array's device address (host code
-// cannot use the symbol itself) and fill the constant part (the request ids 0..max-1).
+std::mutex g_static_mu;
+struct StaticDevice {
+  unsigned long long ctx_id;  // the CUDA context the array was set up in (0: not yet)
+  void* base;                 // device address of okv_static_scratch in that context
+};
+StaticDevice g_static[256] = {};  // per device ordinal
+
+// With the device current: resolve the array's device address (host code cannot use the symbol
+// itself) and, the first time in each CUDA context of the device, fill the constant part (the
+// request ids 0..max-1). A context that was reset and created again (cudaDeviceReset) gets a new
+// context id, so its array is set up again.
 cudaError_t static_scratch(void** base) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 256) return cudaErrorInvalidDevice;
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, okv_static_scratch);  // also makes the device's context current
+  if (e != cudaSuccess) return e;
+  // driver calls through entry points, so the library keeps no link-time dependency on libcuda
+  typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+  typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+  static const CtxGetCurrentFn get_current = reinterpret_cast<CtxGetCurrentFn>(driver_entry("cuCtxGetCurrent"));
+  static const CtxGetIdFn get_id = reinterpret_cast<CtxGetIdFn>(driver_entry("cuCtxGetId"));
+  CUcontext cu = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&cu) != CUDA_SUCCESS || !cu || get_id(cu, &id) != CUDA_SUCCESS)
+    return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_static_mu);
-  if (!g_static_base[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, okv_static_scratch);
-    if (e != cudaSuccess) return e;
+  if (g_static[dev].ctx_id != id || g_static[dev].base != p) {
     unsigned char* b = static_cast<unsigned char*>(p);
     static_init_kernel<<<(kStaticMaxRequests + 255) / 256, 256>>>(
         reinterpret_cast<int32_t*>(b + kStaticIdsOffset), kStaticMaxRequests, reinterpret_cast<int32_t*>(b),
@@ -690,9 +716,10 @@ cudaError_t static_scratch(void** base) {
     e = cudaGetLastError();
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return e;
-    g_static_base[dev] = p;
+    g_static[dev].ctx_id = id;
+    g_static[dev].base = p;
   }
-  *base = g_static_base[dev];
+  *base = p;
   return cudaSuccess;
 }
 
@@ -701,14 +728,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      f = nullptr;
-    return reinterpret_cast<EncodeTiledFn>(f);
-  }();
+  static EncodeTiledFn fn = reinterpret_cast<EncodeTiledFn>(driver_entry("cuTensorMapEncodeTiled"));
   return fn;
 }
 
@@ -735,7 +755,7 @@ extern "C" okv_status okv_attend_static(int32_t n_requests, int32_t q_heads, int
   G.bs = block_size;
   G.kb = slots;
   G.R = n_requests;
-  G.nb_max = 0x3FFFFFFF;  // block ids are checked against each request's length only
+  G.nb_max = (int32_t)(INT32_MAX / block_size);  // block ids are checked against each request's length
   G.dtype = dtype;
   G.elem = dtype == OKV_F32 ? 4 : 2;
   G.block_bytes = (int64_t)2 * block_size * head_dim * G.elem;
@@ -743,6 +763,13 @@ extern "C" okv_status okv_attend_static(int32_t n_requests, int32_t q_heads, int
   // the split partials must fit in the fixed workspace
   if (attend_workspace_bytes(G, n_requests) > kStaticScratchBytes - kStaticPartialsOffset) return OKV_EINVAL;
 
+  // the kernels run on `stream` with the array's address on the current device: both must agree
+  if (stream) {
+    int dev = 0, sdev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaStreamGetDevice((cudaStream_t)stream, &sdev) != cudaSuccess)
+      return OKV_ECUDA;
+    if (sdev != dev) return OKV_EINVAL;
+  }
   void* base = nullptr;
   if (static_scratch(&base) != cudaSuccess) return OKV_ECUDA;
   unsigned char* b = static_cast<unsigned char*>(base);
@@ -769,9 +796,11 @@ extern "C" okv_status okv_attend_static(int32_t n_requests, int32_t q_heads, int
     pmap = &map;
   }
   // the split arrival counters must start at zero (the kernel leaves them at zero, but a call
-  // may follow any earlier one): clear them on the stream first
+  // may follow any earlier one), and the error word starts clear for each call: clear both on
+  // the stream first
   int32_t* arrivals = reinterpret_cast<int32_t*>(b + kStaticArrivalsOffset);
-  if (cudaMemsetAsync(arrivals, 0, (size_t)n_requests * kv_heads * 4, (cudaStream_t)stream) != cudaSuccess)
+  if (cudaMemsetAsync(arrivals, 0, (size_t)n_requests * kv_heads * 4, (cudaStream_t)stream) != cudaSuccess ||
+      cudaMemsetAsync(b, 0, 16, (cudaStream_t)stream) != cudaSuccess)
     return OKV_ECUDA;
   int n_launch = 0, split = 0;
   cudaError_t e = launch_attend(G, S, T, n_requests, 0, q, out, nullptr, nullptr, pmap, b + kStaticPartialsOffset,

@@ -63,6 +63,7 @@ def lib():
             P = ctypes.POINTER(SynthParams)
             i32, i64, vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
             L.synth_fill_kv.argtypes = [vp, P, i32, i32, i32, i32, i32]
+            L.synth_fill_kv_layer.argtypes = [vp, P, i32, i32, i32, i32, i32, i32]
             L.synth_queries.argtypes = [vp, P, i32, i32, i32, i32, vp, vp, i32]
             L.synth_token_kv.argtypes = [vp, vp, P, i32, i32, vp, vp]
             L.synth_direction.argtypes = [vp, P, i32, i32, i32, i32]
@@ -70,8 +71,8 @@ def lib():
             L.synth_block_direction.restype = i32
             L.synth_normals.argtypes = [vp, i64, ctypes.c_uint64, ctypes.c_uint64,
                                         ctypes.c_uint64, ctypes.c_uint64]
-            for f in (L.synth_fill_kv, L.synth_queries, L.synth_token_kv, L.synth_direction,
-                      L.synth_normals):
+            for f in (L.synth_fill_kv, L.synth_fill_kv_layer, L.synth_queries, L.synth_token_kv,
+                      L.synth_direction, L.synth_normals):
                 f.restype = ctypes.c_int
             _lib = L
     return _lib
@@ -190,6 +191,20 @@ def fill_kv(buf_ptr: int, w: Workload, req_key: int, tok_begin: int, tok_end: in
                              tok_end, cap_blocks, nt)
     if rc != 0:
         raise ValueError("synth_fill_kv: bad arguments")
+
+
+def fill_kv_layer(out: np.ndarray, w: Workload, req_key: int, layer: int, tok_begin: int, tok_end: int,
+                  n_threads: int | None = None, plant_blocks: int | None = None) -> None:
+    """Fill one layer of one request into `out`, a C-contiguous [Hkv][cap_blocks][2][bs][d] array
+    of the storage dtype: the bytes fill_kv writes for that layer."""
+    assert out.flags["C_CONTIGUOUS"] and out.dtype == np_dtype(w.dtype)
+    assert out.shape[0] == w.kv_heads and out.shape[2:] == (2, w.block_size, w.head_dim)
+    p = w.params(plant_blocks)
+    nt = n_threads or os.cpu_count() or 1
+    rc = lib().synth_fill_kv_layer(ctypes.c_void_p(_ptr(out)), ctypes.byref(p), req_key, layer, tok_begin,
+                                   tok_end, out.shape[1], nt)
+    if rc != 0:
+        raise ValueError("synth_fill_kv_layer: bad arguments")
 
 
 def queries(w: Workload, layer: int, step: int, kind: int, req_ids, req_keys,

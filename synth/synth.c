@@ -138,7 +138,8 @@ typedef struct {
   void* buf;
   const synth_params* p;
   int32_t req_key, tok_begin, tok_end, cap_blocks;
-  int32_t n_items; /* layers * kv_heads */
+  int32_t layer_begin; /* first layer written; buf starts at that layer */
+  int32_t n_items;     /* (layers written) * kv_heads */
   int32_t tid, n_threads;
 } fill_job;
 
@@ -146,7 +147,7 @@ static void fill_unit(const fill_job* J, int32_t layer, int32_t h) {
   const synth_params* p = J->p;
   const int d = p->head_dim, bs = p->block_size;
   const int64_t unit_elems = (int64_t)J->cap_blocks * 2 * bs * d;
-  const int64_t unit_off = ((int64_t)layer * p->kv_heads + h) * unit_elems;
+  const int64_t unit_off = ((int64_t)(layer - J->layer_begin) * p->kv_heads + h) * unit_elems;
   const int32_t nb_used = (J->tok_end + bs - 1) / bs;
   int32_t* dirs = (int32_t*)malloc(sizeof(int32_t) * (size_t)(nb_used > 0 ? nb_used : 1));
   block_directions(p, layer, J->req_key, h, nb_used, dirs);
@@ -182,22 +183,23 @@ static void fill_unit(const fill_job* J, int32_t layer, int32_t h) {
 static void* fill_worker(void* arg) {
   fill_job* J = (fill_job*)arg;
   for (int32_t it = J->tid; it < J->n_items; it += J->n_threads)
-    fill_unit(J, it / J->p->kv_heads, it % J->p->kv_heads);
+    fill_unit(J, J->layer_begin + it / J->p->kv_heads, it % J->p->kv_heads);
   return NULL;
 }
 
-int synth_fill_kv(void* buf, const synth_params* p, int32_t req_key, int32_t tok_begin,
-                  int32_t tok_end, int32_t cap_blocks, int32_t n_threads) {
+static int fill_layers(void* buf, const synth_params* p, int32_t req_key, int32_t layer_begin,
+                       int32_t n_layers, int32_t tok_begin, int32_t tok_end, int32_t cap_blocks,
+                       int32_t n_threads) {
   if (check_params(p) || !buf || tok_begin < 0 || tok_end < tok_begin ||
       (int64_t)cap_blocks * p->block_size < tok_end)
     return -1;
   if (n_threads < 1) n_threads = 1;
-  const int32_t n_items = p->layers * p->kv_heads;
+  const int32_t n_items = n_layers * p->kv_heads;
   if (n_threads > n_items) n_threads = n_items;
   fill_job* jobs = (fill_job*)malloc(sizeof(fill_job) * (size_t)n_threads);
   pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)n_threads);
   for (int t = 0; t < n_threads; ++t) {
-    fill_job J = {buf, p, req_key, tok_begin, tok_end, cap_blocks, n_items, t, n_threads};
+    fill_job J = {buf, p, req_key, tok_begin, tok_end, cap_blocks, layer_begin, n_items, t, n_threads};
     jobs[t] = J;
   }
   for (int t = 1; t < n_threads; ++t) pthread_create(&th[t], NULL, fill_worker, &jobs[t]);
@@ -206,6 +208,18 @@ int synth_fill_kv(void* buf, const synth_params* p, int32_t req_key, int32_t tok
   free(th);
   free(jobs);
   return 0;
+}
+
+int synth_fill_kv(void* buf, const synth_params* p, int32_t req_key, int32_t tok_begin,
+                  int32_t tok_end, int32_t cap_blocks, int32_t n_threads) {
+  if (check_params(p)) return -1;
+  return fill_layers(buf, p, req_key, 0, p->layers, tok_begin, tok_end, cap_blocks, n_threads);
+}
+
+int synth_fill_kv_layer(void* buf, const synth_params* p, int32_t req_key, int32_t layer,
+                        int32_t tok_begin, int32_t tok_end, int32_t cap_blocks, int32_t n_threads) {
+  if (check_params(p) || layer < 0 || layer >= p->layers) return -1;
+  return fill_layers(buf, p, req_key, layer, 1, tok_begin, tok_end, cap_blocks, n_threads);
 }
 
 /* ---- queries ----------------------------------------------------------------------------- */

@@ -64,6 +64,14 @@ int synth_fill_kv(void* buf, const synth_params* p, int32_t req_key, int32_t tok
                   int32_t tok_end, int32_t cap_blocks, int32_t n_threads);
 
 /*
+ * The same contents as synth_fill_kv writes for one layer: tokens [tok_begin, tok_end) of
+ * layer `layer` into buf laid out [kv_heads][cap_blocks][2][block_size][head_dim].
+ * Returns 0, or -1 on bad arguments.
+ */
+int synth_fill_kv_layer(void* buf, const synth_params* p, int32_t req_key, int32_t layer,
+                        int32_t tok_begin, int32_t tok_end, int32_t cap_blocks, int32_t n_threads);
+
+/*
  * One layer's query (kind 0) or draft query (kind 1) of step `step` for `batch`
  * requests. out: [batch][q_heads][head_dim] in the storage dtype.
  * req_ids[i] is the request id (drives the noise); req_keys[i] its KV content key

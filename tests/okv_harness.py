@@ -1,4 +1,4 @@
-"""Test rig: one okv context (CUDA library) and the CPU oracle over the same host KV bytes.
+"""Test rig: one okv context (CUDA library) and the CPU oracle over the same seeded host KV.
 
 Comparison rules (the method's tolerances):
 * block summaries, slot tables, stamps, fetch lists, pool bytes, lengths: exact;
@@ -9,6 +9,16 @@ Comparison rules (the method's tolerances):
 * attention: max abs error <= 1e-5 (binary32 storage) or 2e-2 (bfloat16 storage);
 * decode-side tiers of partially staged requests (routes, entries in use, kept entry of each
   block): exact; kept copies equal their blocks of the full copy byte for byte.
+
+The oracle keeps its own copy of the host KV (filled from the seeded generator, appended to by
+the oracle itself), so pools, kept copies and attention are compared against bytes the CUDA
+library never wrote. The library's own host writes (appends) are checked directly: after every
+append the token at the appended position must equal the generator's token, and nothing else
+in the blocks around it may have changed.
+
+Selections with exact ties (the oracle's binary32 score of several blocks equal to the K-th
+score bit for bit, e.g. a zero draft query or byte-identical blocks) must follow the lowest-id
+rule exactly; `check_selection(exact=True)` allows no swap at all.
 """
 from __future__ import annotations
 
@@ -43,7 +53,12 @@ def out_to_f64(t, dtype) -> np.ndarray:
 
 class Rig:
     def __init__(self, w: synth.Workload, *, contexts=None, capacity_tokens=None, n_alias=None,
-                 max_requests=None, active=None, layers_kept=None, n_threads=None, local_cap=None):
+                 max_requests=None, active=None, layers_kept=None, n_threads=None, local_cap=None,
+                 edit_kv=None):
+        """edit_kv(layer, key, unit_array): an optional change to the generated input KV of one
+        layer of one content key (array [Hkv][cap_blocks][2][bs][d] of the storage type), applied
+        alike to the library's host buffers and to the oracle's copy (e.g. byte-identical blocks
+        for exact-tie cases)."""
         self.w = w
         B = w.batch
         self.contexts = np.asarray(contexts if contexts is not None else w.contexts(), np.int32)
@@ -71,6 +86,10 @@ class Rig:
                 n_fill = int(max(self.contexts[j] for j in range(B) if self.keys[j] == k))
                 synth.fill_kv(hb.ptr, w, k, 0, n_fill, self.cap_blocks, n_threads=n_threads,
                               plant_blocks=nb_plant)
+                if edit_kv is not None:
+                    view = self._host_view(hb)
+                    for l in range(w.layers):
+                        edit_kv(l, k, view[l])
                 self.bufs[k] = hb
         self.ctx = Context(self.cfg)
         # local_cap[i] >= 0: batch request i is partially staged with that many decode-side
@@ -89,17 +108,32 @@ class Rig:
                 self.local_bufs[i] = lb
             self.ctx.add_request_partial(int(self.ids[i]), full, self.cap_blocks, lb.ptr if lb else 0,
                                          int(self.local_cap[i]), int(self.contexts[i]))
-        # the oracle sees request slot i of the batch (rows of the device arrays = request ids)
+        # the oracle sees request slot i of the batch (rows of the device arrays = request ids); its
+        # host KV is a copy of its own, generated again from the same seeds
+        n_fill_of = {int(k): int(max(self.contexts[j] for j in range(B) if self.keys[j] == k)) for k in self.keys}
+
+        def host_fill(layer, key, arr):
+            synth.fill_kv_layer(arr, w, key, layer, 0, n_fill_of[key], n_threads=n_threads,
+                                plant_blocks=nb_plant)
+            if edit_kv is not None:
+                edit_kv(layer, key, arr)
+
         self.model = oracle.OracleModel(
             layers=w.layers, q_heads=w.q_heads, kv_heads=w.kv_heads, head_dim=w.head_dim,
             block_size=w.block_size, budget_tokens=w.budget_tokens, dtype=w.dtype,
-            req_ptrs=[self.bufs[int(k)].ptr for k in self.keys],
+            host_fill=host_fill, req_keys=self.keys,
             cap_blocks=[self.cap_blocks] * B, n_tok=self.contexts, n_threads=n_threads,
             layers_kept=layers_kept, local_cap=self.local_cap)
         self.sdt = np.float32 if w.dtype == F32 else np.uint16
         # the oracle's routes of partially staged requests, summed over every staging checked
         self.tally = {"local_hits": 0, "local_fills": 0, "full_reads": 0}
         self._summarised = set()  # (layer, batch index) whose oracle summaries are built
+
+    def _host_view(self, hb) -> np.ndarray:
+        """The library's host KV buffer as [L][Hkv][cap_blocks][2][bs][d] storage (no copy)."""
+        w = self.w
+        sdt = np.float32 if w.dtype == F32 else np.uint16
+        return hb.numpy(sdt, (w.layers, w.kv_heads, self.cap_blocks, 2, w.block_size, w.head_dim))
 
     def _ensure_summaries(self, layer: int, requests=None) -> None:
         reqs = range(self.w.batch) if requests is None else requests
@@ -132,9 +166,11 @@ class Rig:
             want = self.model.summ[layer][i][:, :nb]
             assert np.array_equal(gpu[:, :nb], want), f"summaries differ: layer {layer} request {i}"
 
-    def check_selection(self, layer: int, requests=None):
-        """Compare the GPU selection with the oracle's (band rule); return the GPU selection as
-        (ids [B][Hkv][kb], counts [B][Hkv]) in batch order, for re-syncing the oracle."""
+    def check_selection(self, layer: int, requests=None, exact: bool = False):
+        """Compare the GPU selection with the oracle's (band rule; with `exact`, no swap at all:
+        for inputs whose scores tie exactly on both sides by construction, the selection must be
+        the oracle's, ids and order); return the GPU selection as (ids [B][Hkv][kb],
+        counts [B][Hkv]) in batch order, for re-syncing the oracle."""
         counts, ids, scores = self.ctx.read_selection(layer)
         reqs = range(self.w.batch) if requests is None else requests
         B, H, kb = self.w.batch, self.w.kv_heads, self.kb
@@ -160,6 +196,9 @@ class Rig:
                 # GPU scores agree with the oracle's within binary32 summation error
                 assert np.allclose(gs, osc[gsel], rtol=2e-6, atol=1e-6 * max(1.0, float(np.abs(osc).max()))), \
                     (layer, i, h, float(np.abs(gs - osc[gsel]).max()))
+                if exact:
+                    assert np.array_equal(gsel, osel), \
+                        f"selection differs (exact ties): layer {layer} req {i} head {h}: {gsel[:8]}... vs {osel[:8]}..."
                 if not np.array_equal(np.sort(gsel), np.sort(osel)):
                     sK = float(osc[osel[-1]])
                     band = set(np.nonzero(np.abs(osc.astype(np.float64) - sK) <= TIE_REL * abs(sK))[0].tolist())
@@ -257,16 +296,19 @@ class Rig:
 
     # ---- one staging + attention round ---------------------------------------------------------
     def stage(self, layer: int, step: int, cap: float, draft_step: int | None = None, requests=None,
-              check_pool=True):
+              check_pool=True, draft=None, exact=False):
+        """Stage `layer` from the draft of `draft_step` (or the given [B][Hq][d] `draft`) and check
+        selections, tables, tiers and pools against the oracle."""
         import torch
         ds = step - 1 if draft_step is None else draft_step
-        draft = self.batch_queries(layer, ds, 1)
+        if draft is None:
+            draft = self.batch_queries(layer, ds, 1)
         self.ctx.stage(layer, self.device_rows(draft, (self.w.q_heads, self.w.head_dim)), step, cap)
         torch.cuda.synchronize()
         assert self.ctx.sync(60_000) == 0
         self._ensure_summaries(layer, requests)
         self.model.score_topk(layer, draft, requests=requests)
-        gsel, swaps = self.check_selection(layer, requests=requests)
+        gsel, swaps = self.check_selection(layer, requests=requests, exact=exact)
         C = oracle.fetch_cap_blocks(cap, self.kb)
         self.model.select(layer, C, step, sel_override=gsel, requests=requests)
         self.check_tables(layer, requests=requests)
@@ -303,15 +345,65 @@ class Rig:
         return errs, swaps
 
     def append(self, layer: int) -> None:
-        """Append each request's next token (the generator's token at its position)."""
+        """Append each request's next token (the generator's token at its position); check the
+        library's write into its host buffers, then append to the oracle's own copy."""
         import torch
         pos = self.model.n_tok[layer].copy()
         self._ensure_summaries(layer)
         k, v = synth.token_kv(self.w, layer, self.keys, pos, plant_blocks=self.plant_blocks)
         shp = (self.w.kv_heads, self.w.head_dim)
+        snap = self.host_snapshot([layer])
         self.ctx.append(layer, self.device_rows(k, shp), self.device_rows(v, shp))
         torch.cuda.synchronize()
+        assert self.ctx.sync(60_000) == 0
+        self.check_host_append(snap, {layer: (k, v)})
         self.model.append(layer, k, v)
+        self.check_host_tail(layer)
+
+    # ---- the library's host writes (appends) -----------------------------------------------------
+    def host_snapshot(self, layers, requests=None, positions=None):
+        """Copies of the blocks around each request's next token position in the library's host
+        buffers: the blocks of positions pos - 1, pos and pos + 1 (within capacity). positions[l]
+        gives [B] positions per layer (default: the oracle's current lengths)."""
+        reqs = range(self.w.batch) if requests is None else requests
+        bs = self.w.block_size
+        snap = {}
+        for l in layers:
+            for i in reqs:
+                pos = int(self.model.n_tok[l, i] if positions is None else positions[l][i])
+                view = self._host_view(self.bufs[int(self.keys[i])])[l]
+                b0 = max(0, (pos - 1) // bs)
+                b1 = min(self.cap_blocks - 1, (pos + 1) // bs)
+                snap[l, i] = (pos, b0, view[:, b0:b1 + 1].copy())
+        return snap
+
+    def check_host_tail(self, layer: int, requests=None) -> None:
+        """The valid tokens of each request's tail block in the library's host buffer equal the
+        oracle's own copy."""
+        bs = self.w.block_size
+        for i in (range(self.w.batch) if requests is None else requests):
+            n = int(self.model.n_tok[layer, i])
+            if n == 0:
+                continue
+            b, nv = (n - 1) // bs, (n - 1) % bs + 1
+            got = self._host_view(self.bufs[int(self.keys[i])])[layer][:, b, :, :nv]
+            want = np.stack([self.model.host_unit(layer, i, h)[b, :, :nv] for h in range(self.w.kv_heads)])
+            assert np.array_equal(got, want), f"host tail block differs from the oracle's copy: layer {layer} req {i}"
+
+    def check_host_append(self, snap, kv) -> None:
+        """After an append: in every snapshotted window the token at the appended position holds
+        the generator's K and V (kv[layer] = (k [B][Hkv][d], v)) and every other byte is unchanged."""
+        bs = self.w.block_size
+        for (l, i), (pos, b0, before) in snap.items():
+            k, v = kv[l]
+            want = before.copy()
+            want[:, pos // bs - b0, 0, pos % bs] = k[i]
+            want[:, pos // bs - b0, 1, pos % bs] = v[i]
+            got = self._host_view(self.bufs[int(self.keys[i])])[l][:, b0:b0 + before.shape[1]]
+            if not np.array_equal(got, want):
+                bad = np.argwhere(got != want)[0]
+                raise AssertionError(f"host write of the append differs: layer {l} req {i} position {pos}: "
+                                     f"first difference at [head, block - {b0}, k/v, token, dim] = {bad.tolist()}")
 
     def close(self):
         self.ctx.close()

@@ -107,7 +107,8 @@ def test_gqa32b_32k_b32_sampled():
 
 def test_mixed_lengths_appending_all_layers():
     """Reasoning-style mixed lengths (1K-32K, drawn per request) growing by one token per step on
-    all 36 layers through okv_step with appends; sampled units follow the oracle."""
+    all 36 layers through okv_step with appends; the library's host writes of the sampled
+    requests are checked on every layer, and their units on two layers follow the oracle."""
     import torch
     w = synth.WORKLOADS["qwen3_8b_mixed_b64"].scaled(batch=16, steps=6)
     layers = [0, 35]
@@ -136,16 +137,21 @@ def test_mixed_lengths_appending_all_layers():
             q = all_layers(t, 0)
             dr = all_layers(t, 1)
             out = torch.zeros((L, R, Hq, d), dtype=torch_dtype(w.dtype), device="cuda")
+            pos = {l: rig.contexts + t for l in range(L)}
+            snap = rig.host_snapshot(range(L), requests=sample, positions=pos)
             rig.ctx.step(to_device(q, w.dtype), to_device(dr, w.dtype), out, t + 1, k_new=to_device(k_all, w.dtype),
                          v_new=to_device(v_all, w.dtype))
             torch.cuda.synchronize()
             assert rig.ctx.sync(120_000) == 0
+            # the library's host writes, on every layer of the sampled requests
+            rig.check_host_append(snap, {l: (k_all[l], v_all[l]) for l in range(L)})
             for l in layers:
                 for i in sample:  # the oracle appends only what it follows
                     for h in range(Hkv):
                         oracle.append(rig.model.host_unit(l, i, h), rig.model.summ[l][i, h],
                                       int(rig.model.n_tok[l, i]), w.block_size, d, k_all[l, i, h], v_all[l, i, h])
                     rig.model.n_tok[l, i] += 1
+                rig.check_host_tail(l, requests=sample)
                 assert rig.check_attention(l, q[l], out[l], requests=sample) <= ATOL[w.dtype]
                 rig.model.score_topk(l, dr[l], requests=sample)
                 gsel, _ = rig.check_selection(l, requests=sample)

@@ -289,7 +289,8 @@ def test_sync_deadline_reports_timeout():
 def test_step_with_appends_every_unit():
     """okv_step with appends (every layer's append on the library's own stream, each after its
     layer's previous staging) over 20 steps across block boundaries, 3 layers x 3 requests:
-    attention, selections, tables and pools of every unit after every step."""
+    the library's host writes, attention, selections, tables and pools of every unit after every
+    step."""
     import torch
     import oracle as O
     from okv_harness import to_device, torch_dtype
@@ -317,12 +318,15 @@ def test_step_with_appends_every_unit():
             v_all = np.stack([v for _, v in kv])
             q, dr = all_layers(t, 0), all_layers(t, 1)
             out = torch.zeros((L, R, Hq, d), dtype=torch_dtype(w.dtype), device="cuda")
+            snap = rig.host_snapshot(range(L))
             rig.ctx.step(to_device(q, w.dtype), to_device(dr, w.dtype), out, t + 1,
                          k_new=to_device(k_all, w.dtype), v_new=to_device(v_all, w.dtype))
             torch.cuda.synchronize()
             assert rig.ctx.sync(60_000) == 0
+            rig.check_host_append(snap, {l: (k_all[l], v_all[l]) for l in range(L)})
             for l in range(L):
                 rig.model.append(l, k_all[l], v_all[l])
+                rig.check_host_tail(l)
                 assert rig.check_attention(l, q[l], out[l]) <= ATOL[BF16]
                 rig.model.score_topk(l, dr[l])
                 gsel, _ = rig.check_selection(l)

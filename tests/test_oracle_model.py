@@ -98,3 +98,49 @@ def test_driver_matches_per_unit_functions(dtype):
                     assert np.array_equal(bufs[r][l, h], unit), (step, l, r, h)
                     assert np.array_equal(model.summ[l][r, h], u["summ"]), (step, l, r, h)
                     assert int(model.n_tok[l, r]) == u["n"]
+
+
+def test_private_host_copy():
+    """With host_fill the driver keeps its own copy of each (layer, content key): aliased requests
+    share it, appends write only it, and every result equals the driver run on raw buffers
+    holding the same bytes."""
+    rng = np.random.default_rng(5)
+    dtype = oracle.BF16
+    contexts = np.array([60, 60, 90], np.int32)
+    cap = -(-int(contexts.max() + 4) // BS)
+    src = _host(rng, dtype, cap, contexts)
+    keys = [0, 0, 1]  # requests 0 and 1 share one content
+    bufs = [src[0].copy(), src[0].copy(), src[2].copy()]
+    frozen = [b.copy() for b in src]
+    fills = []
+
+    def host_fill(layer, key, arr):
+        fills.append((layer, key))
+        arr[...] = src[2 * key][layer]
+
+    common = dict(layers=L, q_heads=HQ, kv_heads=HKV, head_dim=D, block_size=BS, budget_tokens=BUDGET,
+                  dtype=dtype, cap_blocks=[cap] * 3, n_tok=contexts, n_threads=2)
+    own = oracle.OracleModel(host_fill=host_fill, req_keys=keys, **common)
+    raw = oracle.OracleModel(req_ptrs=[b.ctypes.data for b in bufs], **common)
+    assert sorted(fills) == [(l, k) for l in range(L) for k in (0, 1)]
+    assert own.host_unit_ptr(0, 0, 1) == own.host_unit_ptr(0, 1, 1) != own.host_unit_ptr(0, 2, 1)
+    for l in range(L):
+        for m in (own, raw):
+            m.build_summaries(l)
+        draft = oracle_pins._round(rng.standard_normal((3, HQ, D)), dtype)
+        q = oracle_pins._round(rng.standard_normal((3, HQ, D)), dtype)
+        for m in (own, raw):
+            m.stage(l, draft, KB, 0)
+        assert np.array_equal(own.attend(l, q), raw.attend(l, q))
+        # appends of the non-aliased request only (aliased requests cannot append)
+        k = oracle_pins._round(rng.standard_normal((3, HKV, D)), dtype)
+        v = oracle_pins._round(rng.standard_normal((3, HKV, D)), dtype)
+        for h in range(HKV):
+            oracle.append(own.host_unit(l, 2, h), own.summ[l][2, h], int(own.n_tok[l, 2]), BS, D, k[2, h], v[2, h])
+            oracle.append(raw.host_unit(l, 2, h), raw.summ[l][2, h], int(raw.n_tok[l, 2]), BS, D, k[2, h], v[2, h])
+        own.n_tok[l, 2] += 1
+        raw.n_tok[l, 2] += 1
+        assert np.array_equal(own.host_unit(l, 2, 0), bufs[2][l, 0])
+        assert np.array_equal(own.summ[l], raw.summ[l])
+    # the sources handed to host_fill were never written
+    assert all(np.array_equal(a, b) for a, b in zip(src, frozen))

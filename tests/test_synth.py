@@ -45,6 +45,15 @@ def test_token_kv_matches_fill():
             assert np.array_equal(buf[layer, :, b, 1, t], v[i])
 
 
+def test_one_layer_fill_matches_the_whole_fill():
+    w = synth.WORKLOADS["qwen3_8b_mixed_b64"].scaled(layers=3, batch=2)
+    buf = _fill(w, 4, 77)
+    for layer in range(3):
+        one = np.zeros(buf.shape[1:], dtype=buf.dtype)
+        synth.fill_kv_layer(one, w, 4, layer, 0, 77, n_threads=3)
+        assert np.array_equal(one, buf[layer])
+
+
 def test_planted_blocks_carry_the_direction():
     w = synth.WORKLOADS["qwen3_8b_16k_b128"].scaled(layers=1, dtype=synth.F32)
     buf = _fill(w, 0, 16 * 40)

@@ -31,12 +31,23 @@ def _static_inputs(rig, layer):
 @pytest.mark.parametrize("name,kw", [
     ("qwen_bf16", dict(wl="qwen3_8b_16k_b128", layers=1, batch=3)),      # tensor-core path, split partials
     ("tiny_fp32", dict(wl="tiny")),                                       # CUDA-core path, split partials
+    # tensor-core path, GQA group 4 (half the MMA's columns), the largest split (16 slices of the
+    # 128 slots per unit): the most split partials per unit the workspace bound allows for
+    ("qwen_bf16_split16", dict(wl="qwen3_8b_16k_b128", layers=1, batch=3, split="16")),
+    # CUDA-core path at the largest head dim, fp32
+    ("fp32_d256", dict(wl="qwen3_8b_16k_b128", layers=1, batch=2, dtype=F32, head_dim=256, q_heads=16,
+                       kv_heads=8, context=3000, budget_tokens=512)),
 ])
-def test_static_attention_matches_okv_attend(name, kw):
+def test_static_attention_matches_okv_attend(name, kw, monkeypatch):
     import torch
-    w = synth.WORKLOADS[kw["wl"]]
-    if "layers" in kw:
-        w = w.scaled(layers=kw["layers"], batch=kw["batch"])
+    kw = dict(kw)
+    wl = kw.pop("wl")
+    split = kw.pop("split", None)
+    if split is not None:
+        monkeypatch.setenv("OKV_ATTEND_SPLIT", split)  # read by both entry points at each launch
+    w = synth.WORKLOADS[wl]
+    if kw:
+        w = w.scaled(**kw)
     rig = Rig(w)
     try:
         rig.stage(0, 0, 1.0, draft_step=-1, check_pool=False)
@@ -53,6 +64,8 @@ def test_static_attention_matches_okv_attend(name, kw):
             torch.cuda.synchronize()
             err = float(np.abs(out_to_f64(got, w.dtype) - out_to_f64(ref, w.dtype)).max())
             assert err <= ATOL[w.dtype], (name, call, err)
+            # and against the oracle directly
+            assert rig.check_attention(0, rig.batch_queries(0, step, 0), got) <= ATOL[w.dtype]
     finally:
         rig.close()
 
