@@ -62,8 +62,9 @@ typedef struct {
   int32_t max_requests;           /* request ids are 0 .. max_requests-1 */
   int32_t max_blocks_per_request; /* largest context (in blocks) any request may reach; the
                                      selection keeps a unit's per-block arrays in one CTA's
-                                     shared memory, which bounds it (about 16000 blocks at a
-                                     128-slot budget on GB300; okv_create says the limit) */
+                                     shared memory (6 bytes per block), which bounds it
+                                     (about 37600 blocks, 600K tokens, at a 128-slot budget
+                                     on GB300; okv_create says the limit) */
   float fetch_cap;                /* default fetch cap, a fraction of the budget (0.05) */
   int32_t dtype;                  /* OKV_F32 or OKV_BF16 storage for KV, queries, outputs */
 } okv_config;

@@ -145,9 +145,14 @@ __device__ void score_chunk(const Geom& G, const LayerState& S, int32_t r, int32
 
 // ---- top-K and diff / admit / evict (one unit) ---------------------------------------------
 //
-// Top-K: a radix select over the order-preserving score images finds the K-th largest image T;
-// the blocks at or above T are sorted by (score desc, block id asc) and the first K are the
-// selection (equal scores resolve to the lower block id).
+// Top-K: a most-significant-digit radix select over the order-preserving score images (8-bit
+// digits, warp-aggregated histogram counts) narrows a prefix until the K-th largest image lies
+// in a digit bin that is taken whole, or until the image T itself is known. The selection is
+// then every image above the prefix plus, among the images equal to it, the lowest block ids
+// needed to make K: an ordered compaction in block-id order (warp-contiguous segments, ballot
+// prefix counts) writes them in id order, and each one's place in (score desc, block id asc)
+// order is its rank, counted against the K candidates, so equal scores resolve to the lower
+// block id.
 //
 // Diff / admit / evict: a block -> slot map of the unit's slot table is built in shared memory;
 // hits (selected and resident) keep their slot and get stamp = step; misses are ranked in
@@ -157,16 +162,11 @@ __device__ void score_chunk(const Geom& G, const LayerState& S, int32_t r, int32
 //
 // With pred_ids / pred_n set, only the top-K is computed and written there (prediction only:
 // the unit's selection, slot table and fetch list are left as they are).
-__host__ __device__ inline size_t pow2_at_least(size_t n) {
-  size_t p = 2;
-  while (p < n) p <<= 1;
-  return p;
-}
+__host__ __device__ inline size_t align16(size_t n) { return (n + 15) & ~size_t(15); }
 
 __host__ __device__ inline size_t select_bytes(const Geom& G, int32_t nb_cap) {
-  const size_t kp = pow2_at_least((size_t)nb_cap > (size_t)G.kb ? (size_t)nb_cap : (size_t)G.kb);
-  return kp * 8 + (size_t)G.kb * 8 + (size_t)nb_cap * 4 + 256 * 4 + (((size_t)nb_cap * 2 + 15) & ~size_t(15)) +
-         (size_t)6 * G.kb * 4 + 40 * 4;
+  return (size_t)G.kb * 8 /* tkey */ + (size_t)G.kb * 8 /* candidates */ + (size_t)6 * G.kb * 4 + 48 * 4 +
+         256 * 4 /* histogram */ + align16((size_t)nb_cap * 4) + align16((size_t)nb_cap * 2);
 }
 
 // lcap >= 0: the request is partially staged with a decode-side tier of lcap entries per unit,
@@ -175,23 +175,24 @@ __device__ void select_unit(const Geom& G, const LayerState& S, int32_t r, int32
                             int32_t nb_cap, const uint32_t* ord_in, int32_t cap_blocks, int32_t step,
                             int32_t lcap, Counters* ctr, int32_t* err, uint8_t* smem, int32_t* pred_ids,
                             int32_t* pred_n) {
-  const size_t kp = pow2_at_least((size_t)nb_cap > (size_t)G.kb ? (size_t)nb_cap : (size_t)G.kb);
-  unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem);  // [kp] candidates
-  unsigned long long* tkey = keys + kp;                                    // [kb] eviction order
-  uint32_t* ord = reinterpret_cast<uint32_t*>(tkey + G.kb);                // [nb_cap] score images
-  uint32_t* hist = ord + nb_cap;                                           // [256]
-  int16_t* b2s = reinterpret_cast<int16_t*>(hist + 256);                   // [nb_cap] block -> slot
-  int32_t* sb = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(b2s) + (((size_t)nb_cap * 2 + 15) & ~size_t(15)));
+  // the Kb-sized arrays first: every address below derives from kernel parameters alone
+  unsigned long long* tkey = reinterpret_cast<unsigned long long*>(smem);  // [kb] eviction order
+  uint32_t* ckey = reinterpret_cast<uint32_t*>(tkey + G.kb);  // [kb] selected images, in block-id order
+  int32_t* cid = reinterpret_cast<int32_t*>(ckey + G.kb);     // [kb] their block ids
+  int32_t* sb = cid + G.kb;       // [kb] slot -> block
   int32_t* st = sb + G.kb;        // [kb] stamps
   int32_t* hit = st + G.kb;       // [kb]
   int32_t* target = hit + G.kb;   // [kb]
   int32_t* selid = target + G.kb; // [kb] selection, in order
   int32_t* missrank = selid + G.kb;  // [kb] rank of a miss, or -1
   int32_t* fblk = hit;            // [kb] block of each fetch entry (reuses `hit` once it is read)
-  int32_t* scratch = missrank + G.kb;  // [40]
+  int32_t* scratch = missrank + G.kb;  // [48]
+  uint32_t* hist = reinterpret_cast<uint32_t*>(scratch + 48);  // [256]
+  uint32_t* ord = hist + 256;                                   // [nb_cap] score images
+  int16_t* b2s = reinterpret_cast<int16_t*>(reinterpret_cast<uint8_t*>(ord) + align16((size_t)nb_cap * 4));  // [nb_cap]
 
   const int64_t unit = (int64_t)r * G.Hkv + h;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
   const bool predict = pred_ids != nullptr;
   // the scores were written by the other CTAs of this unit: read them past L1
   for (int32_t b = tid; b < nb; b += blockDim.x) {
@@ -204,7 +205,6 @@ __device__ void select_unit(const Geom& G, const LayerState& S, int32_t r, int32
       st[s] = S.stamp[unit * G.kb + s];
       hit[s] = 0;
     }
-  if (tid == 0) scratch[34] = 0;
   __syncthreads();
   if (!predict)
     for (int32_t s = tid; s < G.kb; s += blockDim.x) {
@@ -213,7 +213,8 @@ __device__ void select_unit(const Geom& G, const LayerState& S, int32_t r, int32
       else if (b >= 0) b2s[b] = (int16_t)s;
     }
 
-  // ---- top-K: radix select of the K-th largest score image T ----
+  // ---- top-K: radix select. Invariant: the K largest images are those whose masked image is
+  // above `prefix` plus the first `krem` (by block id) of those whose masked image equals it ----
   const int32_t K = nb < G.kb ? nb : G.kb;
   uint32_t prefix = 0, mask = 0;
   int32_t krem = K;
@@ -221,19 +222,23 @@ __device__ void select_unit(const Geom& G, const LayerState& S, int32_t r, int32
     for (int shift = 24; shift >= 0; shift -= 8) {
       for (int32_t i = tid; i < 256; i += blockDim.x) hist[i] = 0;
       __syncthreads();
-      for (int32_t b = tid; b < nb; b += blockDim.x) {
-        const uint32_t u = ord[b];
-        if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
+#pragma unroll 1
+      for (int32_t b0 = 0; b0 < nb; b0 += blockDim.x) {
+        const int32_t b = b0 + tid;
+        const uint32_t u = b < nb ? ord[b] : 0u;
+        const bool in = b < nb && (u & mask) == prefix;
+        // lanes with the same digit add once, by their lowest lane (the leading digits of a
+        // unit's scores are mostly equal, and one shared atomic per lane would serialise)
+        const uint32_t dg = in ? ((u >> shift) & 255u) : (256u + (uint32_t)lane);
+        const unsigned grp = __match_any_sync(0xffffffffu, dg);
+        if (in && (__ffs(grp) - 1) == lane) atomicAdd(&hist[dg], (uint32_t)__popc(grp));
       }
       __syncthreads();
       if (warp == 0) {
-        // lane l owns digits 255 - 8l .. 248 - 8l (high to low)
-        uint32_t cnt[8], own = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          cnt[i] = hist[255 - 8 * lane - i];
-          own += cnt[i];
-        }
+        // lane l owns digits 255 - 8l .. 248 - 8l (high to low); the lane whose digits hold the
+        // K-th image walks them again
+        uint32_t own = 0;
+        for (int i = 0; i < 8; ++i) own += hist[255 - 8 * lane - i];
         uint32_t incl = own;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -243,14 +248,15 @@ __device__ void select_unit(const Geom& G, const LayerState& S, int32_t r, int32
         const uint32_t excl = incl - own;
         if (excl < (uint32_t)krem && (uint32_t)krem <= incl) {
           uint32_t run = excl;
-#pragma unroll
           for (int i = 0; i < 8; ++i) {
-            if (run + cnt[i] >= (uint32_t)krem) {
+            const uint32_t c = hist[255 - 8 * lane - i];
+            if (run + c >= (uint32_t)krem) {
               scratch[32] = 255 - 8 * lane - i;
               scratch[33] = krem - (int32_t)run;
+              scratch[34] = (int32_t)c;
               break;
             }
-            run += cnt[i];
+            run += c;
           }
         }
       }
@@ -258,57 +264,83 @@ __device__ void select_unit(const Geom& G, const LayerState& S, int32_t r, int32
       prefix |= (uint32_t)scratch[32] << shift;
       mask |= 255u << shift;
       krem = scratch[33];
+      const bool whole = scratch[34] == krem;  // the bin of the K-th image is taken whole
       __syncthreads();
+      if (whole) break;
     }
   }
-  // candidates: every block at or above T (all of them when the budget covers the context)
-  for (int32_t b = tid; b < nb; b += blockDim.x) {
-    const uint32_t u = ord[b];
-    if (K >= nb || u >= prefix) {
-      const int32_t pos = atomicAdd(&scratch[34], 1);
-      keys[pos] = ((unsigned long long)u << 32) | (unsigned long long)(~(uint32_t)b);
+  // ---- ordered compaction, in block-id order: every image above the prefix, and the first krem
+  // equal to it. Warp w walks blocks [w*seg, (w+1)*seg) twice: counts, then places ----
+  {
+    const int32_t seg = (((nb + nwarps - 1) / nwarps) + 31) & ~31;
+    const int32_t lo = warp * seg, hi = min(nb, lo + seg);
+    const unsigned below = (1u << lane) - 1u;
+    int32_t n_eq = 0, n_gt = 0;
+#pragma unroll 1
+    for (int32_t b0 = lo; b0 < hi; b0 += 32) {
+      const int32_t b = b0 + lane;
+      const uint32_t m = b < hi ? (ord[b] & mask) : 0u;
+      n_eq += __popc(__ballot_sync(0xffffffffu, b < hi && m == prefix));
+      n_gt += __popc(__ballot_sync(0xffffffffu, b < hi && m > prefix));
     }
-  }
-  __syncthreads();
-  const int32_t n_cand = scratch[34];
-  const int32_t cp = (int32_t)pow2_at_least((size_t)n_cand);
-  for (int32_t i = n_cand + tid; i < cp; i += blockDim.x) keys[i] = 0ull;
-  __syncthreads();
-  for (int32_t k = 2; k <= cp; k <<= 1) {  // bitonic sort, descending
-    for (int32_t j = k >> 1; j > 0; j >>= 1) {
-      for (int32_t i = tid; i < cp; i += blockDim.x) {
-        const int32_t ixj = i ^ j;
-        if (ixj > i) {
-          const unsigned long long x = keys[i], y = keys[ixj];
-          if (((i & k) == 0) ? (x < y) : (x > y)) {
-            keys[i] = y;
-            keys[ixj] = x;
-          }
-        }
+    if (lane == 0) {
+      scratch[warp] = n_eq;
+      scratch[16 + warp] = n_gt;
+    }
+    __syncthreads();
+    int32_t eq_base = 0, gt_base = 0;
+    for (int w = 0; w < warp; ++w) {
+      eq_base += scratch[w];
+      gt_base += scratch[16 + w];
+    }
+#pragma unroll 1
+    for (int32_t b0 = lo; b0 < hi; b0 += 32) {
+      const int32_t b = b0 + lane;
+      const uint32_t u = b < hi ? ord[b] : 0u;
+      const uint32_t m = u & mask;
+      const bool eq = b < hi && m == prefix, gt = b < hi && m > prefix;
+      const unsigned beq = __ballot_sync(0xffffffffu, eq), bgt = __ballot_sync(0xffffffffu, gt);
+      const int32_t eb = eq_base + __popc(beq & below), gb = gt_base + __popc(bgt & below);
+      if (gt || (eq && eb < krem)) {
+        const int32_t pos = gb + min(eb, krem);
+        ckey[pos] = u;
+        cid[pos] = b;
       }
-      __syncthreads();
+      eq_base += __popc(beq);
+      gt_base += __popc(bgt);
     }
   }
-  if (predict) {
-    for (int32_t i = tid; i < K; i += blockDim.x)
-      pred_ids[unit * G.kb + i] = (int32_t)(~(uint32_t)(keys[i] & 0xFFFFFFFFull));
-    if (tid == 0) pred_n[unit] = K;
-    return;
-  }
+  __syncthreads();
+  // ---- order: the rank of candidate i in (image desc, block id asc); candidates are in id order,
+  // so an equal image ranks before i exactly when its candidate index is lower ----
   for (int32_t i = tid; i < K; i += blockDim.x) {
-    const unsigned long long k = keys[i];
-    const int32_t b = (int32_t)(~(uint32_t)(k & 0xFFFFFFFFull));
-    selid[i] = b;
-    S.sel_ids[unit * G.kb + i] = b;
-    S.sel_scores[unit * G.kb + i] = from_orderable((uint32_t)(k >> 32));
+    const uint32_t u = ckey[i];
+    const int32_t b = cid[i];
+    int32_t rank = 0;
+#pragma unroll 4
+    for (int32_t j = 0; j < K; ++j) {
+      const uint32_t x = ckey[j];
+      rank += (x > u) | ((x == u) & (j < i));
+    }
+    if (predict) {
+      pred_ids[unit * G.kb + rank] = b;
+      continue;
+    }
+    selid[rank] = b;
+    S.sel_ids[unit * G.kb + rank] = b;
+    S.sel_scores[unit * G.kb + rank] = from_orderable(u);
     const int32_t s = b2s[b];
     if (s >= 0) {
       hit[s] = 1;
       st[s] = step;
-      missrank[i] = -1;
+      missrank[rank] = -1;
     } else {
-      missrank[i] = 0;
+      missrank[rank] = 0;
     }
+  }
+  if (predict) {
+    if (tid == 0) pred_n[unit] = K;
+    return;
   }
   if (tid == 0) S.n_sel[unit] = K;
   __syncthreads();
@@ -424,9 +456,11 @@ stage_kernel(Geom G, LayerState S, ReqTables RT, int32_t chunks, int32_t nb_cap,
   if (bad && threadIdx.x == 0 && chunk == 0) record_error(err, kErrLength, -1, r, len);
   if (!bad && b_lo < nb)
     score_chunk<T>(G, S, r, h, b_lo, min(nb, b_lo + kScoreChunk), draft, ord, reinterpret_cast<float*>(smem + 16));
-  __threadfence();
+  // the barrier orders every thread's score images before thread 0's device-scope fence, which
+  // then releases them all ahead of the arrival (one fence per CTA instead of one per thread)
   __syncthreads();
   if (threadIdx.x == 0) {
+    __threadfence();
     last = atomicAdd(&arrivals[ua], 1) == chunks - 1;
     if (last) arrivals[ua] = 0;
   }

@@ -101,9 +101,9 @@ def test_largest_budget_batch_one():
 
 
 def test_longest_context_at_the_default_budget():
-    """256000 tokens (16000 blocks, near the largest context one staging CTA's shared memory
-    holds at a 128-slot budget), one request, cap 0.05."""
-    w = QWEN.scaled(layers=1, batch=1, context=256000)
+    """600000 tokens (37500 blocks, near the largest context one staging CTA's shared memory
+    holds at a 128-slot budget: 37680 blocks), one request, cap 0.05."""
+    w = QWEN.scaled(layers=1, batch=1, context=600000)
     rig = Rig(w)
     try:
         errs, _ = rig.run_steps(2, 0.05)

@@ -144,7 +144,7 @@ def test_api_errors():
     with pytest.raises(OkvError):
         Context(Config(1, 8, 2, 100, 16, 2048, 2, 64))  # head_dim not a multiple of 32
     with pytest.raises(OkvError) as e:  # the selection's on-chip arrays would exceed shared memory
-        Context(Config(1, 8, 2, 64, 16, 512, 1, 32767))
+        Context(Config(1, 8, 2, 64, 16, 512, 1, 40000))
     assert e.value.status == binding.EINVAL
     cfg = Config(1, 8, 2, 64, 16, 512, 2, 8, 1.0, F32)
     ctx = Context(cfg)
