@@ -326,7 +326,8 @@ okv_status okv_create(const okv_config* cfg, okv_ctx** out) {
   if (k.budget_tokens < k.block_size || k.budget_tokens % k.block_size) return bad("budget must be a multiple of block_size");
   if (k.budget_tokens / k.block_size > 1024) return bad("at most 1024 slots per unit");
   if (k.max_requests <= 0 || k.max_blocks_per_request <= 0) return bad("sizes");
-  if (k.max_blocks_per_request > 32767) return bad("max_blocks_per_request must be at most 32767");
+  if ((int64_t)k.max_blocks_per_request * k.block_size > INT32_MAX)
+    return bad("max_blocks_per_request * block_size must fit in 32 bits (token positions)");
   if (!(k.fetch_cap > 0.f) || k.fetch_cap > 1.f) return bad("fetch_cap must be in (0, 1]");
   if (k.dtype != OKV_F32 && k.dtype != OKV_BF16) return bad("dtype");
   c->cfg = k;
