@@ -555,18 +555,28 @@ cudaError_t run_mma(const Geom& G, const LayerState& S, const ReqTables& T, int3
   return cudaGetLastError();
 }
 
+// The largest split whose partials ([units x split][rows][d + 2] binary32) fit `ws_bytes`, at
+// most `want` (the split is chosen at each launch, e.g. from OKV_ATTEND_SPLIT, while the
+// workspace was sized when it was allocated).
+int32_t fit_split(const Geom& G, int32_t n_active, int32_t nrows, int32_t want, size_t ws_bytes) {
+  const size_t per = (size_t)n_active * G.Hkv * nrows * (G.d + 2) * sizeof(float);
+  int32_t split = want;
+  while (split > 1 && per * (size_t)split > ws_bytes) --split;
+  return split;
+}
+
 // One attention launch over `nrows` rows (the group's heads of q, then, if dq is given, of dq).
 cudaError_t launch_rows(const Geom& G, const LayerState& S, const ReqTables& T, int32_t n_active,
                         int32_t layer, const void* q, const void* dq, void* out, void* dout, int32_t nrows,
-                        const CUtensorMap* pool_map, void* partials, int32_t* arrivals, Counters* ctr,
-                        int32_t* err, cudaStream_t s, int32_t* used_split) {
+                        const CUtensorMap* pool_map, void* partials, size_t ws_bytes, int32_t* arrivals,
+                        Counters* ctr, int32_t* err, cudaStream_t s, int32_t* used_split) {
   cudaError_t e;
   int32_t split;
   if (use_mma(G)) {
     const Rows<__nv_bfloat16> rows{(const __nv_bfloat16*)q, (const __nv_bfloat16*)dq, (__nv_bfloat16*)out,
                                    (__nv_bfloat16*)dout, nrows};
     const MmaShape sh = mma_shape();
-    split = pick_split(G, n_active, 2, sh.nw);
+    split = fit_split(G, n_active, nrows, pick_split(G, n_active, 2, sh.nw), ws_bytes);
     if (sh.nw == 8 && sh.ns == 2)
       e = run_mma<8, 2>(G, S, T, n_active, layer, rows, pool_map, partials, arrivals, ctr, err, s, split);
     else if (sh.nw == 8 && sh.ns == 3)
@@ -578,7 +588,7 @@ cudaError_t launch_rows(const Geom& G, const LayerState& S, const ReqTables& T, 
     else
       e = run_mma<4, 3>(G, S, T, n_active, layer, rows, pool_map, partials, arrivals, ctr, err, s, split);
   } else {
-    split = pick_split(G, n_active, 4, kSimtWarps);
+    split = fit_split(G, n_active, nrows, pick_split(G, n_active, 4, kSimtWarps), ws_bytes);
     const size_t smem = (size_t)(G.kb + 32) * 4 + (size_t)kSimtWarps * nrows * (G.d + 2) * 4;
     const int grid = n_active * G.Hkv * split;
     if (G.dtype == OKV_F32) {
@@ -615,8 +625,8 @@ size_t attend_workspace_bytes(const Geom& G, int32_t n_active) {
 
 cudaError_t launch_attend(const Geom& G, const LayerState& S, const ReqTables& T, int32_t n_active,
                           int32_t layer, const void* q, void* out, const void* dq, void* dout,
-                          const CUtensorMap* pool_map, void* partials, int32_t* arrivals, Counters* ctr,
-                          int32_t* err, cudaStream_t s, int* n_launches, int* used_split) {
+                          const CUtensorMap* pool_map, void* partials, size_t ws_bytes, int32_t* arrivals,
+                          Counters* ctr, int32_t* err, cudaStream_t s, int* n_launches, int* used_split) {
   *n_launches = 0;
   *used_split = 0;
   if (n_active <= 0) return cudaSuccess;
@@ -624,16 +634,16 @@ cudaError_t launch_attend(const Geom& G, const LayerState& S, const ReqTables& T
   if (!dq || 2 * G.g <= kMaxG) {
     // one pass: the draft heads (if any) ride in the MMA's spare columns next to the query heads
     e = launch_rows(G, S, T, n_active, layer, q, dq, out, dout, dq ? 2 * G.g : G.g, pool_map, partials,
-                    arrivals, ctr, err, s, used_split);
+                    ws_bytes, arrivals, ctr, err, s, used_split);
     if (e != cudaSuccess) return e;
     *n_launches = 1;
   } else {
     // a group too wide for both: two passes over the resident set
-    e = launch_rows(G, S, T, n_active, layer, q, nullptr, out, nullptr, G.g, pool_map, partials, arrivals,
-                    ctr, err, s, used_split);
+    e = launch_rows(G, S, T, n_active, layer, q, nullptr, out, nullptr, G.g, pool_map, partials, ws_bytes,
+                    arrivals, ctr, err, s, used_split);
     if (e != cudaSuccess) return e;
-    e = launch_rows(G, S, T, n_active, layer, dq, nullptr, dout, nullptr, G.g, pool_map, partials, arrivals,
-                    ctr, err, s, used_split);
+    e = launch_rows(G, S, T, n_active, layer, dq, nullptr, dout, nullptr, G.g, pool_map, partials, ws_bytes,
+                    arrivals, ctr, err, s, used_split);
     if (e != cudaSuccess) return e;
     *n_launches = 2;
   }
@@ -804,7 +814,8 @@ extern "C" okv_status okv_attend_static(int32_t n_requests, int32_t q_heads, int
     return OKV_ECUDA;
   int n_launch = 0, split = 0;
   cudaError_t e = launch_attend(G, S, T, n_requests, 0, q, out, nullptr, nullptr, pmap, b + kStaticPartialsOffset,
-                                arrivals, reinterpret_cast<Counters*>(b + 16), reinterpret_cast<int32_t*>(b),
+                                kStaticScratchBytes - kStaticPartialsOffset, arrivals,
+                                reinterpret_cast<Counters*>(b + 16), reinterpret_cast<int32_t*>(b),
                                 (cudaStream_t)stream, &n_launch, &split);
   return e == cudaSuccess ? OKV_OK : OKV_ECUDA;
 }

@@ -799,7 +799,8 @@ okv_status attend_impl(okv_ctx* c, const char* who, int32_t layer, const void* q
   int n_launch = 0, split = 0;
   Timer t(c, OKV_K_ATTEND, s);
   OKV_CUDA(c, okv::launch_attend(G, S, T, n_active, layer, q, out, dq, dout, c->have_map ? &c->pool_map : nullptr,
-                                 c->partials, c->attend_arrivals, c->ctr_dev, c->err_dev, s, &n_launch, &split));
+                                 c->partials, c->partials_bytes, c->attend_arrivals, c->ctr_dev, c->err_dev, s,
+                                 &n_launch, &split));
   t.stop(n_launch);
   return OKV_OK;
 }

@@ -110,13 +110,14 @@ cudaError_t launch_gather(const Geom& G, const LayerState& S, const ReqTables& T
 // path; `partials` is a workspace of at least attend_workspace_bytes() bytes.
 size_t attend_workspace_bytes(const Geom& G, int32_t n_active);
 // `arrivals`: [n_active * Hkv] int32 split arrival counters that start at zero and are left at
-// zero; the last CTA of a split unit merges the partials.
+// zero; the last CTA of a split unit merges the partials. `ws_bytes` is the size of `partials`:
+// a launch never splits a unit more than its partials fit.
 // With a draft query `dq` (look-ahead attention), its heads attend over the same resident set and
 // write `dout`: in the same pass when 2g <= 8, else in a second pass.
 cudaError_t launch_attend(const Geom& G, const LayerState& S, const ReqTables& T, int32_t n_active,
                           int32_t layer, const void* q, void* out, const void* dq, void* dout,
-                          const CUtensorMap* pool_map, void* partials, int32_t* arrivals, Counters* ctr,
-                          int32_t* err, cudaStream_t s, int* n_launches, int* used_split);
+                          const CUtensorMap* pool_map, void* partials, size_t ws_bytes, int32_t* arrivals,
+                          Counters* ctr, int32_t* err, cudaStream_t s, int* n_launches, int* used_split);
 bool attend_uses_tensor_cores(const Geom& G);
 
 }  // namespace okv

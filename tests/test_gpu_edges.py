@@ -110,3 +110,18 @@ def test_longest_context_at_the_default_budget():
         assert max(errs) <= ATOL[BF16]
     finally:
         rig.close()
+
+
+def test_split_chosen_after_create(monkeypatch):
+    """The attention's split may be chosen after the context sized its split workspace (here
+    OKV_ATTEND_SPLIT=16 set after okv_create, whose 1024 units call for a split of 2): each launch
+    splits no further than the workspace holds, and the outputs still match the oracle."""
+    w = QWEN.scaled(layers=1, batch=128, context=1040)
+    rig = Rig(w, n_alias=4)
+    try:
+        monkeypatch.setenv("OKV_ATTEND_SPLIT", "16")
+        sample = [0, 77, 127]
+        errs, _ = rig.run_steps(2, 0.05, requests=sample, check_pool=False)
+        assert max(errs) <= ATOL[BF16]
+    finally:
+        rig.close()
