@@ -65,12 +65,16 @@ struct okv_ctx {
   uint8_t* draft_buf = nullptr;  // [layers][R][Hq][d]: the staging's own copy of the draft queries
   uint32_t* scores = nullptr;    // [R][Hkv][nb_max]: block score images of the layer being staged
   int32_t* stage_arrivals = nullptr;   // [R * Hkv]: scoring CTAs finished per unit (kept at zero)
+  // second staging lane (odd layers), when OKV_STAGE_LANES=2: its own stream and workspace
+  uint32_t* scores2 = nullptr;
+  int32_t* stage_arrivals2 = nullptr;
   int32_t* attend_arrivals = nullptr;  // [R * Hkv]: attention split CTAs finished per unit
   int32_t* append_arrivals = nullptr;  // [layers][R]: append CTAs finished per request (kept at zero)
   int32_t* gather_work = nullptr;      // [layers][2]: gather work and exit counters (kept at zero)
   uint8_t* step_drafts = nullptr;      // [2][layers][R][Hq][d]: okv_step's copies of its drafts
   int step_parity = 0;                 // which half of step_drafts the next okv_step fills
   cudaEvent_t ev_step_read[2] = {nullptr, nullptr};  // the stagings of the last step using each half
+  cudaEvent_t ev_step_read2[2] = {nullptr, nullptr}; // ... on the second staging lane
   bool step_used[2] = {false, false};
   bool stage_on_caller = false;  // run scoring/selection on the caller's stream (see okv_create)
   CUtensorMap pool_map;  // 64-byte aligned by its type
@@ -88,6 +92,7 @@ struct okv_ctx {
 
   // streams and events
   cudaStream_t sel_stream = nullptr, copy_stream = nullptr;
+  cudaStream_t sel_stream2 = nullptr;        // the second staging lane, or NULL
   cudaStream_t app_stream = nullptr;         // okv_step's appends, ahead of the caller's stream
   std::vector<cudaEvent_t> ev_appended;      // [layers]: the last append of each layer
   cudaEvent_t ev_in = nullptr;
@@ -216,6 +221,7 @@ okv_status check_device_error(okv_ctx* c) {
 okv_status sync_internal(okv_ctx* c) {
   OKV_CUDA(c, cudaStreamSynchronize(c->app_stream));
   OKV_CUDA(c, cudaStreamSynchronize(c->sel_stream));
+  if (c->sel_stream2) OKV_CUDA(c, cudaStreamSynchronize(c->sel_stream2));
   OKV_CUDA(c, cudaStreamSynchronize(c->copy_stream));
   return OKV_OK;
 }
@@ -283,6 +289,7 @@ okv_status okv_host_free(void* p) {
 void okv_destroy(okv_ctx* c) {
   if (!c) return;
   if (c->sel_stream) cudaStreamSynchronize(c->sel_stream);
+  if (c->sel_stream2) cudaStreamSynchronize(c->sel_stream2);
   if (c->copy_stream) cudaStreamSynchronize(c->copy_stream);
   if (c->app_stream) cudaStreamSynchronize(c->app_stream);
   for (auto& t : c->pending) {
@@ -295,12 +302,15 @@ void okv_destroy(okv_ctx* c) {
   for (auto e : c->ev_appended) if (e) cudaEventDestroy(e);
   if (c->ev_in) cudaEventDestroy(c->ev_in);
   for (auto e : c->ev_step_read) if (e) cudaEventDestroy(e);
+  for (auto e : c->ev_step_read2) if (e) cudaEventDestroy(e);
   if (c->sel_stream) cudaStreamDestroy(c->sel_stream);
+  if (c->sel_stream2) cudaStreamDestroy(c->sel_stream2);
   if (c->copy_stream) cudaStreamDestroy(c->copy_stream);
   if (c->app_stream) cudaStreamDestroy(c->app_stream);
   void* bufs[] = {c->summ, c->pool, c->slot_block, c->stamp, c->sel_ids, c->sel_scores,
                   c->n_sel, c->fetch, c->n_fetch, c->len, c->active_dev, c->host_kv_dev, c->cap_dev,
                   c->err_dev, c->ctr_dev, c->partials, c->draft_buf, c->scores, c->stage_arrivals, c->attend_arrivals,
+                  c->scores2, c->stage_arrivals2,
                   c->local_of, c->local_used, c->route, c->local_kv_dev, c->local_cap_dev,
                   c->append_arrivals, c->step_drafts, c->gather_work};
   for (void* p : bufs)
@@ -395,6 +405,14 @@ okv_status okv_create(const okv_config* cfg, okv_ctx** out) {
             alloc((void**)&c->local_cap_dev, G.R * 4) && alloc((void**)&c->append_arrivals, (size_t)L * G.R * 4) &&
             alloc((void**)&c->step_drafts, (size_t)2 * L * G.R * G.Hq * G.d * G.elem) &&
             alloc((void**)&c->gather_work, (size_t)L * 2 * 4);
+  // Staging lanes: odd layers stage on a second stream with a workspace of its own, so one layer's
+  // per-unit selection tails overlap the next layer's scoring (measured on GB300: +3% decode
+  // tok/s at the 32B-class shapes, the same at Qwen3-8B batch 128). OKV_STAGE_LANES=1 keeps one.
+  const char* plane = getenv("OKV_STAGE_LANES");
+  const bool two_lanes = !(plane && strcmp(plane, "1") == 0);
+  if (ok && two_lanes)
+    ok = alloc((void**)&c->scores2, (size_t)U * G.nb_max * sizeof(uint32_t)) &&
+         alloc((void**)&c->stage_arrivals2, (size_t)U * 4);
   if (ok) {
     size_t ws = 0;
     for (int32_t n = 1; n <= G.R; ++n) {
@@ -419,6 +437,7 @@ okv_status okv_create(const okv_config* cfg, okv_ctx** out) {
   ck(cudaMemset(c->len, 0, L * G.R * 4));
   ck(cudaMemset(c->err_dev, 0, 16));
   ck(cudaMemset(c->stage_arrivals, 0, U * 4));
+  if (c->stage_arrivals2) ck(cudaMemset(c->stage_arrivals2, 0, U * 4));
   ck(cudaMemset(c->attend_arrivals, 0, U * 4));
   ck(cudaMemset(c->ctr_dev, 0, sizeof(Counters)));
   ck(cudaMemset(c->host_kv_dev, 0, G.R * 8));
@@ -447,10 +466,12 @@ okv_status okv_create(const okv_config* cfg, okv_ctx** out) {
   const char* ps = getenv("OKV_STAGE_STREAM");
   c->stage_on_caller = ps && strcmp(ps, "caller") == 0;
   ck(cudaStreamCreateWithPriority(&c->sel_stream, cudaStreamNonBlocking, prio));
+  if (c->scores2) ck(cudaStreamCreateWithPriority(&c->sel_stream2, cudaStreamNonBlocking, prio));
   ck(cudaStreamCreateWithPriority(&c->copy_stream, cudaStreamNonBlocking, hi));
   ck(cudaStreamCreateWithPriority(&c->app_stream, cudaStreamNonBlocking, hi));
   ck(cudaEventCreateWithFlags(&c->ev_in, cudaEventDisableTiming));
   for (auto& e : c->ev_step_read) ck(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+  for (auto& e : c->ev_step_read2) ck(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
   c->ev_selected.assign(G.L, nullptr);
   c->ev_staged.assign(G.L, nullptr);
   c->ev_appended.assign(G.L, nullptr);
@@ -728,7 +749,10 @@ okv_status stage_impl(okv_ctx* c, int32_t layer, const void* draft_q, bool copie
   cudaStream_t s = (cudaStream_t)stream;
   const LayerState S = layer_state(c, layer);
   const ReqTables T = req_tables(c);
-  cudaStream_t ss = c->sel_stream;
+  const bool lane2 = c->sel_stream2 && (layer & 1);
+  cudaStream_t ss = lane2 ? c->sel_stream2 : c->sel_stream;
+  uint32_t* scores_ws = lane2 ? c->scores2 : c->scores;
+  int32_t* arrivals_ws = lane2 ? c->stage_arrivals2 : c->stage_arrivals;
   const void* draft_src = draft_q;
   if (copied && !c->stage_on_caller) {
     // scoring and selection follow the caller's work so far (its attention of this layer)
@@ -755,8 +779,8 @@ okv_status stage_impl(okv_ctx* c, int32_t layer, const void* draft_q, bool copie
   {
     Timer t(c, OKV_K_SCORE_TOPK, ss);
     int n = 0;
-    OKV_CUDA(c, okv::launch_stage(G, S, T, n_active, max_blocks_at(c, layer), draft_src, c->scores,
-                                  c->stage_arrivals, C, step, c->ctr_dev, c->err_dev, ss, &n));
+    OKV_CUDA(c, okv::launch_stage(G, S, T, n_active, max_blocks_at(c, layer), draft_src, scores_ws, arrivals_ws, C,
+                                  step, c->ctr_dev, c->err_dev, ss, &n));
     t.stop(n);
   }
   OKV_CUDA(c, cudaEventRecord(c->ev_selected[layer], ss));
@@ -863,7 +887,10 @@ okv_status okv_step(okv_ctx* c, const void* q, const void* draft_q, void* out, c
   const bool copied = !c->stage_on_caller;
   if (copied) {
     uint8_t* dst = c->step_drafts + (size_t)p * G.L * qbytes;
-    if (c->step_used[p]) OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_step_read[p], 0));
+    if (c->step_used[p]) {
+      OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_step_read[p], 0));
+      if (c->sel_stream2) OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_step_read2[p], 0));
+    }
     OKV_CUDA(c, cudaMemcpyAsync(dst, draft_q, (size_t)G.L * qbytes, cudaMemcpyDeviceToDevice, s));
     drafts = dst;
     c->step_parity ^= 1;
@@ -891,6 +918,7 @@ okv_status okv_step(okv_ctx* c, const void* q, const void* draft_q, void* out, c
   }
   if (copied) {
     OKV_CUDA(c, cudaEventRecord(c->ev_step_read[p], c->sel_stream));
+    if (c->sel_stream2) OKV_CUDA(c, cudaEventRecord(c->ev_step_read2[p], c->sel_stream2));
     c->step_used[p] = true;
   }
   return OKV_OK;
@@ -903,6 +931,10 @@ okv_status okv_join(okv_ctx* c, void* stream) {
   OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_in, 0));
   OKV_CUDA(c, cudaEventRecord(c->ev_in, c->sel_stream));
   OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_in, 0));
+  if (c->sel_stream2) {
+    OKV_CUDA(c, cudaEventRecord(c->ev_in, c->sel_stream2));
+    OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_in, 0));
+  }
   OKV_CUDA(c, cudaEventRecord(c->ev_in, c->copy_stream));
   OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_in, 0));
   return OKV_OK;
@@ -911,9 +943,10 @@ okv_status okv_join(okv_ctx* c, void* stream) {
 okv_status okv_sync(okv_ctx* c, int64_t timeout_ms) {
   if (!c) return OKV_EINVAL;
   // one event at the end of each internal stream (staging, gather, appends of okv_step)
-  cudaStream_t streams[3] = {c->sel_stream, c->copy_stream, c->app_stream};
-  cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
-  for (int i = 0; i < 3; ++i) {
+  cudaStream_t streams[4] = {c->sel_stream, c->copy_stream, c->app_stream, c->sel_stream2};
+  const int ns = c->sel_stream2 ? 4 : 3;
+  cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
+  for (int i = 0; i < ns; ++i) {
     OKV_CUDA(c, cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming));
     OKV_CUDA(c, cudaEventRecord(ev[i], streams[i]));
   }
@@ -922,7 +955,7 @@ okv_status okv_sync(okv_ctx* c, int64_t timeout_ms) {
   for (;;) {
     bool done = true;
     cudaError_t bad = cudaSuccess;
-    for (int i = 0; i < 3; ++i) {
+    for (int i = 0; i < ns; ++i) {
       const cudaError_t q = cudaEventQuery(ev[i]);
       if (q == cudaErrorNotReady) done = false;
       else if (q != cudaSuccess) bad = q;
@@ -939,7 +972,8 @@ okv_status okv_sync(okv_ctx* c, int64_t timeout_ms) {
     }
     std::this_thread::sleep_for(std::chrono::microseconds(50));
   }
-  for (auto e : ev) cudaEventDestroy(e);
+  for (auto e : ev)
+    if (e) cudaEventDestroy(e);
   if (st != OKV_OK) return st;
   return check_device_error(c);
 }
