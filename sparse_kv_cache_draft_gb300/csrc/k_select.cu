@@ -195,9 +195,19 @@ __device__ void select_unit(const Geom& G, const LayerState& S, int32_t r, int32
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
   const bool predict = pred_ids != nullptr;
   // the scores were written by the other CTAs of this unit: read them past L1
+  uint32_t all_or = 0u, all_and = ~0u;  // bits set in some / every image of the unit
   for (int32_t b = tid; b < nb; b += blockDim.x) {
-    ord[b] = __ldcg(ord_in + unit * G.nb_max + b);
+    const uint32_t u = __ldcg(ord_in + unit * G.nb_max + b);
+    ord[b] = u;
     b2s[b] = -1;
+    all_or |= u;
+    all_and &= u;
+  }
+  all_or = __reduce_or_sync(0xffffffffu, all_or);
+  all_and = __reduce_and_sync(0xffffffffu, all_and);
+  if (lane == 0) {
+    scratch[24 + warp] = (int32_t)all_or;
+    scratch[36 + warp] = (int32_t)all_and;
   }
   if (!predict)
     for (int32_t s = tid; s < G.kb; s += blockDim.x) {
@@ -214,12 +224,26 @@ __device__ void select_unit(const Geom& G, const LayerState& S, int32_t r, int32
     }
 
   // ---- top-K: radix select. Invariant: the K largest images are those whose masked image is
-  // above `prefix` plus the first `krem` (by block id) of those whose masked image equals it ----
+  // above `prefix` plus the first `krem` (by block id) of those whose masked image equals it.
+  // The bits above the highest bit in which the unit's images differ are common to all of them,
+  // so the digits start there (8 bits at a time); when every image is equal no digit is needed ----
   const int32_t K = nb < G.kb ? nb : G.kb;
   uint32_t prefix = 0, mask = 0;
   int32_t krem = K;
   if (K < nb) {
-    for (int shift = 24; shift >= 0; shift -= 8) {
+    uint32_t any = 0u, every = ~0u;
+    for (int w = 0; w < nwarps; ++w) {
+      any |= (uint32_t)scratch[24 + w];
+      every &= (uint32_t)scratch[36 + w];
+    }
+    const uint32_t differ = any ^ every;
+    const int top0 = differ ? 31 - __clz(differ) : -1;
+    // the bits above top0 (every bit if no two images differ)
+    mask = top0 < 0 ? ~0u : (top0 >= 31 ? 0u : ~((2u << top0) - 1u));
+    prefix = every & mask;
+    for (int top = top0; top >= 0;) {
+      const int lo = top >= 7 ? top - 7 : 0;
+      const uint32_t dmask = (2u << (top - lo)) - 1u;  // the digit's bits, shifted down to bit 0
       for (int32_t i = tid; i < 256; i += blockDim.x) hist[i] = 0;
       __syncthreads();
 #pragma unroll 1
@@ -229,7 +253,7 @@ __device__ void select_unit(const Geom& G, const LayerState& S, int32_t r, int32
         const bool in = b < nb && (u & mask) == prefix;
         // lanes with the same digit add once, by their lowest lane (the leading digits of a
         // unit's scores are mostly equal, and one shared atomic per lane would serialise)
-        const uint32_t dg = in ? ((u >> shift) & 255u) : (256u + (uint32_t)lane);
+        const uint32_t dg = in ? ((u >> lo) & dmask) : (256u + (uint32_t)lane);
         const unsigned grp = __match_any_sync(0xffffffffu, dg);
         if (in && (__ffs(grp) - 1) == lane) atomicAdd(&hist[dg], (uint32_t)__popc(grp));
       }
@@ -261,12 +285,13 @@ __device__ void select_unit(const Geom& G, const LayerState& S, int32_t r, int32
         }
       }
       __syncthreads();
-      prefix |= (uint32_t)scratch[32] << shift;
-      mask |= 255u << shift;
+      prefix |= (uint32_t)scratch[32] << lo;
+      mask |= dmask << lo;
       krem = scratch[33];
       const bool whole = scratch[34] == krem;  // the bin of the K-th image is taken whole
       __syncthreads();
       if (whole) break;
+      top = lo - 1;
     }
   }
   // ---- ordered compaction, in block-id order: every image above the prefix, and the first krem
@@ -313,15 +338,23 @@ __device__ void select_unit(const Geom& G, const LayerState& S, int32_t r, int32
   __syncthreads();
   // ---- order: the rank of candidate i in (image desc, block id asc); candidates are in id order,
   // so an equal image ranks before i exactly when its candidate index is lower ----
-  for (int32_t i = tid; i < K; i += blockDim.x) {
-    const uint32_t u = ckey[i];
-    const int32_t b = cid[i];
+  // (with K at most half the CTA, two threads count the ranks of one candidate, half each)
+  const bool pairs = 2 * K <= (int32_t)blockDim.x;
+  for (int32_t i0 = 0; i0 < K; i0 += pairs ? (int32_t)blockDim.x / 2 : (int32_t)blockDim.x) {
+    const int32_t i = i0 + (pairs ? tid >> 1 : tid);
+    const int32_t j0 = pairs && (tid & 1) ? K / 2 : 0, j1 = pairs && !(tid & 1) ? K / 2 : K;
+    const uint32_t u = i < K ? ckey[i] : 0u;
     int32_t rank = 0;
+    if (i < K) {
 #pragma unroll 4
-    for (int32_t j = 0; j < K; ++j) {
-      const uint32_t x = ckey[j];
-      rank += (x > u) | ((x == u) & (j < i));
+      for (int32_t j = j0; j < j1; ++j) {
+        const uint32_t x = ckey[j];
+        rank += (x > u) | ((x == u) & (j < i));
+      }
     }
+    if (pairs) rank += __shfl_xor_sync(0xffffffffu, rank, 1);
+    if (i >= K || (pairs && (tid & 1))) continue;
+    const int32_t b = cid[i];
     if (predict) {
       pred_ids[unit * G.kb + rank] = b;
       continue;
@@ -369,12 +402,19 @@ __device__ void select_unit(const Geom& G, const LayerState& S, int32_t r, int32
   }
   __syncthreads();
   if (n_admit > 0) {
-    for (int32_t s = tid; s < G.kb; s += blockDim.x) {
-      const unsigned long long mine = tkey[s];
-      if (mine == ~0ull) continue;
+    // each slot's rank among the targets (two threads per slot when the slots fill half the CTA)
+    const bool tpairs = 2 * G.kb <= (int32_t)blockDim.x;
+    for (int32_t s0 = 0; s0 < G.kb; s0 += tpairs ? (int32_t)blockDim.x / 2 : (int32_t)blockDim.x) {
+      const int32_t s = s0 + (tpairs ? tid >> 1 : tid);
+      const int32_t o0 = tpairs && (tid & 1) ? G.kb / 2 : 0, o1 = tpairs && !(tid & 1) ? G.kb / 2 : G.kb;
+      const unsigned long long mine = s < G.kb ? tkey[s] : ~0ull;
       int32_t pos = 0;
-      for (int32_t o = 0; o < G.kb; ++o) pos += tkey[o] < mine;
-      if (pos < n_admit) target[pos] = s;
+      if (mine != ~0ull) {
+#pragma unroll 4
+        for (int32_t o = o0; o < o1; ++o) pos += tkey[o] < mine;
+      }
+      if (tpairs) pos += __shfl_xor_sync(0xffffffffu, pos, 1);
+      if (s < G.kb && mine != ~0ull && !(tpairs && (tid & 1)) && pos < n_admit) target[pos] = s;
     }
   }
   __syncthreads();
