@@ -1095,14 +1095,16 @@ def run_partial(args, dist: Dist):
 def run_append(args, dist: Dist):
     """Decode steps that append one token per request and layer: the mixed-length workload
     (contexts ~ U[1K, 32K], one token per step), through okv_step with k_new / v_new. Appends go
-    to each request's own host buffer (requests sharing a buffer cannot append), so the batch is
-    32 by default to fit the host's memory."""
+    to each request's own host buffer (requests sharing a buffer cannot append): at batch 64 and
+    256 steps that is 150 GB of page-locked host memory (a 199 GB GB300 host holds it)."""
     import numpy as np
     import torch
     import synth
     from sparse_kv_cache_draft_gb300 import BF16, Config, Context, HostBuffer
     name = args.workload or "qwen3_8b_mixed_b64"
-    w = synth.WORKLOADS[name].scaled(batch=args.batch or 32)
+    w = synth.WORKLOADS[name]
+    if args.batch:
+        w = w.scaled(batch=args.batch)
     if args.layers:
         w = w.scaled(layers=args.layers)
     B, L, Hq, Hkv, d, bs = w.batch, w.layers, w.q_heads, w.kv_heads, w.head_dim, w.block_size
@@ -1124,21 +1126,32 @@ def run_append(args, dist: Dist):
     for r in range(B):
         ctx.add_request(r, bufs[r].ptr, caps[r], int(ctx0[r]))
     shape_q, shape_kv = (L, B, Hq, d), (L, B, Hkv, d)
-    qh = np.empty((n_steps,) + shape_q, np.uint16)
-    dh = np.empty((n_steps + 1,) + shape_q, np.uint16)
-    kh = np.empty((n_steps,) + shape_kv, np.uint16)
+    # every step's inputs go straight to device memory, one step at a time on the host (the
+    # host's memory holds the requests' KV)
+    q = torch.empty((n_steps,) + shape_q, dtype=torch.bfloat16, device="cuda")
+    dr = torch.empty((n_steps + 1,) + shape_q, dtype=torch.bfloat16, device="cuda")
+    kn = torch.empty((n_steps,) + shape_kv, dtype=torch.bfloat16, device="cuda")
+    vn = torch.empty_like(kn)
+    qh = np.empty(shape_q, np.uint16)
+    kh = np.empty(shape_kv, np.uint16)
     vh = np.empty_like(kh)
-    for t in range(-1, n_steps):
-        for l in range(L):
-            if t >= 0:
-                synth.queries(w, l, t, 0, ids, ids, out=qh[t, l], n_threads=threads)
-                kh[t, l], vh[t, l] = synth.token_kv(w, l, ids, ctx0 + t * grow)
-            synth.queries(w, l, t, 1, ids, ids, out=dh[t + 1, l], n_threads=threads)
 
     def conv(a):
-        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to("cuda")
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
 
-    q, dr, kn, vn = conv(qh), conv(dh), conv(kh), conv(vh)
+    t0 = time.time()
+    for t in range(-1, n_steps):
+        for l in range(L):
+            synth.queries(w, l, t, 1, ids, ids, out=qh[l], n_threads=threads)
+        dr[t + 1].copy_(conv(qh))
+        if t >= 0:
+            for l in range(L):
+                synth.queries(w, l, t, 0, ids, ids, out=qh[l], n_threads=threads)
+                kh[l], vh[l] = synth.token_kv(w, l, ids, ctx0 + t * grow)
+            q[t].copy_(conv(qh))
+            kn[t].copy_(conv(kh))
+            vn[t].copy_(conv(vh))
+    log(f"inputs for {n_steps} steps generated in {time.time() - t0:.1f}s")
     out = torch.empty(shape_q, dtype=torch.bfloat16, device="cuda")
     for l in range(L):
         ctx.stage(l, dr[0, l], 0, 1.0)
