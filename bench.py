@@ -718,6 +718,8 @@ def run_okv(args, dist: Dist):
                                                  "passes over every layer after the timed regions"}},
         "scoring_roofline": {"bound": "hbm", "kernel": "block scoring + top-K", "achieved": round(sc_gbs, 1),
                              "peak": hbm_peak, "unit": "GB/s", "frac": round(sc_gbs / hbm_peak, 4),
+                             "traffic": profiled_traffic("stage_kernel_qwen3_8b_16k.md")
+                             if (wl.name, B) == (WORKLOAD, 128) else None,
                              "bytes_per_launch": int(sc_bytes), "ms_per_launch": round(sc_ms, 5),
                              "note": "in the step the kernel runs on a least-priority stream: its event time "
                                      "includes waiting for SMs the attention holds",
