@@ -139,8 +139,9 @@ OKV_API okv_status okv_append(okv_ctx* ctx, int32_t layer, const void* k_new, co
  *   diff against the resident pool: admit at most C = max(1, floor(cap * Kb)) missing blocks
  *   per unit, evicting least-recently-selected unselected blocks, stamps = step,
  *   gather of the admitted blocks from host memory into their slots.
- * fetch_cap < 0 uses the config's cap. The draft is copied on `stream` before the call returns
- * control of it, so the caller may overwrite draft_q by work enqueued later on `stream`.
+ * fetch_cap < 0 uses the config's cap. The scoring's coefficients are computed from the draft
+ * on `stream` (per KV head and coordinate, the sums of the group's negative and of its positive
+ * draft coordinates), so the caller may overwrite draft_q by work enqueued later on `stream`.
  * Returns once enqueued; okv_attend on the same layer waits for it. */
 OKV_API okv_status okv_stage(okv_ctx* ctx, int32_t layer, const void* draft_q, int32_t step,
                      float fetch_cap, void* stream);
@@ -175,7 +176,8 @@ OKV_API okv_status okv_attend_lookahead(okv_ctx* ctx, int32_t layer, const void*
  * later layers). The result is that of: for l = 0 .. layers-1: okv_append(l) if k_new is not NULL,
  * okv_attend(l), okv_stage(l, step). q, draft_q, out: device [layers][max_requests][q_heads]
  * [head_dim]; k_new, v_new: device [layers][max_requests][kv_heads][head_dim] or NULL.
- * Scheduling: every layer's draft is copied once, up front. Every layer's append is enqueued
+ * Scheduling: the scoring coefficients of every layer's draft are computed in one launch, up
+ * front, on `stream`. Every layer's append is enqueued
  * up front on an internal stream, each after that layer's previous staging. On `stream`, the
  * attention of layer l waits only for the append of layer l. The inputs may be reused by work
  * enqueued on `stream` after the call. Stops at the first failing check (before any work is
@@ -223,8 +225,10 @@ OKV_API okv_status okv_read_local(okv_ctx* ctx, int32_t layer, int32_t* local_us
 
 /* ---- measurement ---- */
 
+/* Kernel kinds of okv_timing: OKV_K_COEF is the scoring's coefficients of the draft queries
+ * (okv_stage, okv_step and okv_predict compute them before the staging); OKV_K_COMBINE is unused. */
 enum {
-  OKV_K_SUMMARY = 0, OKV_K_SCORE_TOPK = 1, OKV_K_SELECT = 2, OKV_K_GATHER = 3, OKV_K_ATTEND = 4,
+  OKV_K_SUMMARY = 0, OKV_K_SCORE_TOPK = 1, OKV_K_COEF = 2, OKV_K_GATHER = 3, OKV_K_ATTEND = 4,
   OKV_K_COMBINE = 5, OKV_K_APPEND = 6, OKV_K_COUNT = 7
 };
 

@@ -16,7 +16,7 @@ import numpy as np
 
 F32, BF16 = 0, 1
 OK, EINVAL, ENOMEM, ECUDA, EDEVICE, ETIMEOUT, ESTATE = range(7)
-KERNEL_KINDS = ("summary", "score_topk", "select", "gather", "attend", "combine", "append")
+KERNEL_KINDS = ("summary", "score_topk", "coef", "gather", "attend", "combine", "append")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lock = threading.Lock()

@@ -47,36 +47,47 @@ __device__ __forceinline__ int32_t block_rank(bool flag, int32_t* scratch, int32
 //
 // Score of block b for KV head h: sum over the g query heads of the group of
 // sum_c max(q_c kmin_c, q_c kmax_c) = sum_c (P_c kmax_c + N_c kmin_c), P_c (N_c) being the sum
-// of the group's positive (negative) query coordinates. One CTA scores up to kScoreChunk blocks
-// of one unit: each warp takes 8 blocks at a time, one 16-byte load per lane per block of the
-// block's [kmin | kmax] record (2d elements) with the lane's coefficients in registers, and
-// reduces the 8 block sums across the warp. The order-preserving 32-bit image of each
+// of the group's positive (negative) query coordinates, computed once per unit by coef_kernel.
+// One CTA scores up to kScoreChunk blocks of one unit: each warp takes 8 blocks at a time, one
+// 16-byte load per lane per block of the block's [kmin | kmax] record (2d elements) with the
+// lane's coefficients in registers, and reduces the 8 block sums across the warp. The order-preserving 32-bit image of each
 // binary32 score goes to `ord_out`. (Staging the chunk through shared memory with one bulk TMA
 // copy was measured slower: its 64 KiB buffer leaves 3 scoring CTAs per SM and the selection
 // tails hold them.)
 constexpr int kScoreChunk = 128;
 constexpr int kStageThreads = 256;
 
-__host__ __device__ inline size_t coef_bytes(const Geom& G) { return ((size_t)2 * G.d * 4 + 15) & ~size_t(15); }
-
+// Coefficients of the factorised score, per unit (layer, request, KV head): N_c (sum of the
+// group's negative draft coordinates c) then P_c (of its positive ones), [2d] binary32, summed
+// over the group's heads in head order. One CTA per (layer, active request), one thread per
+// coordinate and KV head.
 template <typename T>
-__device__ void score_chunk(const Geom& G, const LayerState& S, int32_t r, int32_t h, int32_t b_lo,
-                            int32_t b_hi, const T* __restrict__ draft, uint32_t* __restrict__ ord_out,
-                            float* coef) {
-  constexpr int V = 16 / sizeof(T);
-  const int64_t unit = (int64_t)r * G.Hkv + h;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-  for (int32_t c = tid; c < G.d; c += blockDim.x) {
+__global__ void coef_kernel(Geom G, const int32_t* __restrict__ active, const T* __restrict__ draft,
+                            float* __restrict__ coef, int64_t draft_layer_stride, int64_t coef_layer_stride) {
+  const int32_t a = blockIdx.x, layer = blockIdx.y;
+  const int32_t r = active[a];
+  const T* dq = draft + layer * draft_layer_stride + (int64_t)r * G.Hq * G.d;
+  float* out = coef + layer * coef_layer_stride + (int64_t)r * G.Hkv * 2 * G.d;
+  for (int32_t i = threadIdx.x; i < G.Hkv * G.d; i += blockDim.x) {
+    const int32_t h = i / G.d, c = i % G.d;
     float p = 0.f, n = 0.f;
     for (int32_t j = 0; j < G.g; ++j) {
-      const float x = to_f(draft[((int64_t)r * G.Hq + h * G.g + j) * G.d + c]);
+      const float x = to_f(dq[(int64_t)(h * G.g + j) * G.d + c]);
       p += x > 0.f ? x : 0.f;
       n += x < 0.f ? x : 0.f;
     }
-    coef[c] = n;
-    coef[G.d + c] = p;
+    out[(int64_t)h * 2 * G.d + c] = n;
+    out[(int64_t)h * 2 * G.d + G.d + c] = p;
   }
-  __syncthreads();
+}
+
+template <typename T>
+__device__ void score_chunk(const Geom& G, const LayerState& S, int32_t r, int32_t h, int32_t b_lo,
+                            int32_t b_hi, const float* __restrict__ coef, uint32_t* __restrict__ ord_out) {
+  constexpr int V = 16 / sizeof(T);
+  const int64_t unit = (int64_t)r * G.Hkv + h;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  coef += unit * 2 * G.d;  // this unit's [N | P]
   const int32_t nvec = 2 * G.d / V;  // 16-byte vectors per summary record
   const T* summ = reinterpret_cast<const T*>(S.summ) + unit * G.nb_max * 2 * G.d;
   uint32_t* ord = ord_out + unit * G.nb_max;
@@ -86,7 +97,7 @@ __device__ void score_chunk(const Geom& G, const LayerState& S, int32_t r, int32
     constexpr int U = 8;
     float cf[V];
 #pragma unroll
-    for (int e = 0; e < V; ++e) cf[e] = lane < nvec ? coef[lane * V + e] : 0.f;
+    for (int e = 0; e < V; ++e) cf[e] = lane < nvec ? __ldg(coef + lane * V + e) : 0.f;
     for (int32_t b0 = b_lo + warp * U; b0 < b_hi; b0 += nwarps * U) {
       union {
         uint4 u4;
@@ -135,7 +146,7 @@ __device__ void score_chunk(const Geom& G, const LayerState& S, int32_t r, int32
       x.u4 = __ldcs(reinterpret_cast<const uint4*>(summ + (int64_t)b * 2 * G.d) + v);
       const float* cf = coef + v * V;
 #pragma unroll
-      for (int e = 0; e < V; ++e) part = fmaf(cf[e], to_f(x.e[e]), part);
+      for (int e = 0; e < V; ++e) part = fmaf(__ldg(cf + e), to_f(x.e[e]), part);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
@@ -481,7 +492,7 @@ __device__ void select_unit(const Geom& G, const LayerState& S, int32_t r, int32
 template <typename T>
 __global__ void __launch_bounds__(kStageThreads)
 stage_kernel(Geom G, LayerState S, ReqTables RT, int32_t chunks, int32_t nb_cap,
-             const T* __restrict__ draft, uint32_t* __restrict__ ord, int32_t* __restrict__ arrivals,
+             const float* __restrict__ coef, uint32_t* __restrict__ ord, int32_t* __restrict__ arrivals,
              int32_t cap_blocks, int32_t step, Counters* ctr, int32_t* err, int32_t* pred_ids,
              int32_t* pred_n) {
   extern __shared__ __align__(16) uint8_t smem[];
@@ -495,7 +506,7 @@ stage_kernel(Geom G, LayerState S, ReqTables RT, int32_t chunks, int32_t nb_cap,
   const bool bad = len < 0 || nb > G.nb_max || nb > nb_cap;
   if (bad && threadIdx.x == 0 && chunk == 0) record_error(err, kErrLength, -1, r, len);
   if (!bad && b_lo < nb)
-    score_chunk<T>(G, S, r, h, b_lo, min(nb, b_lo + kScoreChunk), draft, ord, reinterpret_cast<float*>(smem + 16));
+    score_chunk<T>(G, S, r, h, b_lo, min(nb, b_lo + kScoreChunk), coef, ord);
   // the barrier orders every thread's score images before thread 0's device-scope fence, which
   // then releases them all ahead of the arrival (one fence per CTA instead of one per thread)
   __syncthreads();
@@ -514,13 +525,25 @@ stage_kernel(Geom G, LayerState S, ReqTables RT, int32_t chunks, int32_t nb_cap,
 }  // namespace
 
 size_t stage_smem_bytes(const Geom& G, int32_t nb_cap) {
-  const size_t need_score = 16 + coef_bytes(G);
-  const size_t need_select = 16 + select_bytes(G, nb_cap > 0 ? nb_cap : 1);
-  return need_score > need_select ? need_score : need_select;
+  return 16 + select_bytes(G, nb_cap > 0 ? nb_cap : 1);
+}
+
+cudaError_t launch_coef(const Geom& G, const int32_t* active, int32_t n_active, int32_t layers, const void* draft,
+                        int64_t draft_layer_stride, float* coef, int64_t coef_layer_stride, cudaStream_t s) {
+  if (n_active <= 0 || layers <= 0) return cudaSuccess;
+  const dim3 grid((unsigned)n_active, (unsigned)layers);
+  const int threads = G.Hkv * G.d < 256 ? ((G.Hkv * G.d + 31) / 32) * 32 : 256;
+  if (G.dtype == OKV_F32)
+    coef_kernel<float><<<grid, threads, 0, s>>>(G, active, (const float*)draft, coef, draft_layer_stride,
+                                                coef_layer_stride);
+  else
+    coef_kernel<__nv_bfloat16><<<grid, threads, 0, s>>>(G, active, (const __nv_bfloat16*)draft, coef,
+                                                        draft_layer_stride, coef_layer_stride);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_stage(const Geom& G, const LayerState& S, const ReqTables& T, int32_t n_active,
-                         int32_t max_nb, const void* draft, uint32_t* scores, int32_t* arrivals,
+                         int32_t max_nb, const float* coef, uint32_t* scores, int32_t* arrivals,
                          int32_t cap_blocks, int32_t step, Counters* ctr, int32_t* err, cudaStream_t s,
                          int* n_launches, int32_t* pred_ids, int32_t* pred_n) {
   *n_launches = 0;
@@ -533,14 +556,13 @@ cudaError_t launch_stage(const Geom& G, const LayerState& S, const ReqTables& T,
   if (G.dtype == OKV_F32) {
     e = cudaFuncSetAttribute(stage_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    stage_kernel<float><<<grid, kStageThreads, smem, s>>>(G, S, T, chunks, nb_cap, (const float*)draft, scores,
-                                                          arrivals, cap_blocks, step, ctr, err, pred_ids, pred_n);
+    stage_kernel<float><<<grid, kStageThreads, smem, s>>>(G, S, T, chunks, nb_cap, coef, scores, arrivals,
+                                                          cap_blocks, step, ctr, err, pred_ids, pred_n);
   } else {
     e = cudaFuncSetAttribute(stage_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    stage_kernel<__nv_bfloat16><<<grid, kStageThreads, smem, s>>>(
-        G, S, T, chunks, nb_cap, (const __nv_bfloat16*)draft, scores, arrivals, cap_blocks, step, ctr, err,
-        pred_ids, pred_n);
+    stage_kernel<__nv_bfloat16><<<grid, kStageThreads, smem, s>>>(G, S, T, chunks, nb_cap, coef, scores, arrivals,
+                                                                  cap_blocks, step, ctr, err, pred_ids, pred_n);
   }
   e = cudaGetLastError();
   if (e == cudaSuccess) *n_launches = 1;

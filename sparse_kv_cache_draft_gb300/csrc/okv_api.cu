@@ -62,7 +62,8 @@ struct okv_ctx {
   Counters* ctr_dev = nullptr;
   void* partials = nullptr;
   size_t partials_bytes = 0;
-  uint8_t* draft_buf = nullptr;  // [layers][R][Hq][d]: the staging's own copy of the draft queries
+  float* coef_buf = nullptr;     // [layers][R][Hkv][2d]: okv_stage's scoring coefficients of each layer
+  float* pred_coef = nullptr;    // [R][Hkv][2d]: okv_predict's
   uint32_t* scores = nullptr;    // [R][Hkv][nb_max]: block score images of the layer being staged
   int32_t* stage_arrivals = nullptr;   // [R * Hkv]: scoring CTAs finished per unit (kept at zero)
   // second staging lane (odd layers), when OKV_STAGE_LANES=2: its own stream and workspace
@@ -71,8 +72,8 @@ struct okv_ctx {
   int32_t* attend_arrivals = nullptr;  // [R * Hkv]: attention split CTAs finished per unit
   int32_t* append_arrivals = nullptr;  // [layers][R]: append CTAs finished per request (kept at zero)
   int32_t* gather_work = nullptr;      // [layers][2]: gather work and exit counters (kept at zero)
-  uint8_t* step_drafts = nullptr;      // [2][layers][R][Hq][d]: okv_step's copies of its drafts
-  int step_parity = 0;                 // which half of step_drafts the next okv_step fills
+  float* step_coef = nullptr;          // [2][layers][R][Hkv][2d]: okv_step's coefficients of its drafts
+  int step_parity = 0;                 // which half of step_coef the next okv_step fills
   cudaEvent_t ev_step_read[2] = {nullptr, nullptr};  // the stagings of the last step using each half
   cudaEvent_t ev_step_read2[2] = {nullptr, nullptr}; // ... on the second staging lane
   bool step_used[2] = {false, false};
@@ -309,10 +310,10 @@ void okv_destroy(okv_ctx* c) {
   if (c->app_stream) cudaStreamDestroy(c->app_stream);
   void* bufs[] = {c->summ, c->pool, c->slot_block, c->stamp, c->sel_ids, c->sel_scores,
                   c->n_sel, c->fetch, c->n_fetch, c->len, c->active_dev, c->host_kv_dev, c->cap_dev,
-                  c->err_dev, c->ctr_dev, c->partials, c->draft_buf, c->scores, c->stage_arrivals, c->attend_arrivals,
+                  c->err_dev, c->ctr_dev, c->partials, c->coef_buf, c->pred_coef, c->scores, c->stage_arrivals, c->attend_arrivals,
                   c->scores2, c->stage_arrivals2,
                   c->local_of, c->local_used, c->route, c->local_kv_dev, c->local_cap_dev,
-                  c->append_arrivals, c->step_drafts, c->gather_work};
+                  c->append_arrivals, c->step_coef, c->gather_work};
   for (void* p : bufs)
     if (p) cudaFree(p);
   delete c;
@@ -397,13 +398,14 @@ okv_status okv_create(const okv_config* cfg, okv_ctx** out) {
             alloc((void**)&c->active_dev, G.R * 4) && alloc((void**)&c->host_kv_dev, G.R * 8) &&
             alloc((void**)&c->cap_dev, G.R * 4) && alloc((void**)&c->err_dev, 16) &&
             alloc((void**)&c->ctr_dev, sizeof(Counters)) &&
-            alloc((void**)&c->draft_buf, (size_t)L * G.R * G.Hq * G.d * G.elem) &&
+            alloc((void**)&c->coef_buf, (size_t)L * U * 2 * G.d * sizeof(float)) &&
+            alloc((void**)&c->pred_coef, (size_t)U * 2 * G.d * sizeof(float)) &&
             alloc((void**)&c->scores, (size_t)U * G.nb_max * sizeof(uint32_t)) &&
             alloc((void**)&c->stage_arrivals, (size_t)U * 4) && alloc((void**)&c->attend_arrivals, (size_t)U * 4) &&
             alloc((void**)&c->local_of, (size_t)L * U * G.nb_max * 4) && alloc((void**)&c->local_used, (size_t)L * U * 4) &&
             alloc((void**)&c->route, (size_t)L * U * G.kb * 4) && alloc((void**)&c->local_kv_dev, G.R * 8) &&
             alloc((void**)&c->local_cap_dev, G.R * 4) && alloc((void**)&c->append_arrivals, (size_t)L * G.R * 4) &&
-            alloc((void**)&c->step_drafts, (size_t)2 * L * G.R * G.Hq * G.d * G.elem) &&
+            alloc((void**)&c->step_coef, (size_t)2 * L * U * 2 * G.d * sizeof(float)) &&
             alloc((void**)&c->gather_work, (size_t)L * 2 * 4);
   // Staging lanes: odd layers stage on a second stream with a workspace of its own, so one layer's
   // per-unit selection tails overlap the next layer's scoring (measured on GB300: +3% decode
@@ -734,13 +736,14 @@ okv_status okv_append(okv_ctx* c, int32_t layer, const void* k_new, const void* 
 
 namespace {
 
-// `copied`: draft_q is already the library's own copy (okv_step copies every layer's draft at
-// once), so no per-layer copy is made and only the caller's work so far is waited for.
-okv_status stage_impl(okv_ctx* c, int32_t layer, const void* draft_q, bool copied, int32_t step, float fetch_cap,
-                      void* stream) {
+// `coef_ready`: the layer's scoring coefficients, already computed from the draft by okv_step
+// (for every layer at once); NULL: compute them here from draft_q, on the caller's stream, so the
+// caller may reuse its draft buffer. Only the caller's work so far is waited for.
+okv_status stage_impl(okv_ctx* c, int32_t layer, const void* draft_q, const float* coef_ready, int32_t step,
+                      float fetch_cap, void* stream) {
   const Geom& G = c->G;
   if (layer < 0 || layer >= G.L) return fail(c, OKV_EINVAL, "okv_stage: layer %d out of range", layer);
-  if (!draft_q) return fail(c, OKV_EINVAL, "okv_stage: NULL draft query");
+  if (!draft_q && !coef_ready) return fail(c, OKV_EINVAL, "okv_stage: NULL draft query");
   const float cap = fetch_cap < 0.f ? c->cfg.fetch_cap : fetch_cap;
   if (!(cap > 0.f) || cap > 1.f) return fail(c, OKV_EINVAL, "okv_stage: fetch cap %g not in (0, 1]", cap);
   const int32_t C = cap_to_blocks(cap, G.kb);
@@ -753,33 +756,34 @@ okv_status stage_impl(okv_ctx* c, int32_t layer, const void* draft_q, bool copie
   cudaStream_t ss = lane2 ? c->sel_stream2 : c->sel_stream;
   uint32_t* scores_ws = lane2 ? c->scores2 : c->scores;
   int32_t* arrivals_ws = lane2 ? c->stage_arrivals2 : c->stage_arrivals;
-  const void* draft_src = draft_q;
-  if (copied && !c->stage_on_caller) {
-    // scoring and selection follow the caller's work so far (its attention of this layer)
-    OKV_CUDA(c, cudaEventRecord(c->ev_in, s));
-    OKV_CUDA(c, cudaStreamWaitEvent(ss, c->ev_in, 0));
-    if (c->staged_once[layer]) OKV_CUDA(c, cudaStreamWaitEvent(ss, c->ev_staged[layer], 0));
-  } else if (c->stage_on_caller) {
+  const float* coef = coef_ready;
+  if (!coef_ready) {
+    // the coefficients of this layer's draft, on the caller's stream after the previous staging of
+    // this layer has read the layer's coefficient buffer
+    float* dst = c->coef_buf + (size_t)layer * c->per_layer_units * 2 * G.d;
+    if (c->staged_once[layer] && !c->stage_on_caller) OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_selected[layer], 0));
+    {
+      Timer t(c, OKV_K_COEF, s);
+      OKV_CUDA(c, okv::launch_coef(G, c->active_dev, n_active, 1, draft_q, 0, dst, 0, s));
+      t.stop(1);
+    }
+    coef = dst;
+  }
+  if (c->stage_on_caller) {
     // scoring and selection follow the caller's attention of this layer on its own stream
     ss = s;
     if (c->staged_once[layer]) OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_staged[layer], 0));
   } else {
-    // the staging reads the draft later, on the select stream: take a copy on the caller's
-    // stream (after the previous staging of this layer has read its copy) so the caller may
-    // reuse its buffer
-    const size_t qbytes = (size_t)G.R * G.Hq * G.d * G.elem;
-    uint8_t* draft_copy = c->draft_buf + (size_t)layer * qbytes;
-    if (c->staged_once[layer]) OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_selected[layer], 0));
-    OKV_CUDA(c, cudaMemcpyAsync(draft_copy, draft_q, qbytes, cudaMemcpyDeviceToDevice, s));
+    // scoring and selection follow the caller's work so far (its attention of this layer and the
+    // coefficients)
     OKV_CUDA(c, cudaEventRecord(c->ev_in, s));
     OKV_CUDA(c, cudaStreamWaitEvent(ss, c->ev_in, 0));
     if (c->staged_once[layer]) OKV_CUDA(c, cudaStreamWaitEvent(ss, c->ev_staged[layer], 0));
-    draft_src = draft_copy;
   }
   {
     Timer t(c, OKV_K_SCORE_TOPK, ss);
     int n = 0;
-    OKV_CUDA(c, okv::launch_stage(G, S, T, n_active, max_blocks_at(c, layer), draft_src, scores_ws, arrivals_ws, C,
+    OKV_CUDA(c, okv::launch_stage(G, S, T, n_active, max_blocks_at(c, layer), coef, scores_ws, arrivals_ws, C,
                                   step, c->ctr_dev, c->err_dev, ss, &n));
     t.stop(n);
   }
@@ -803,7 +807,7 @@ extern "C" {
 okv_status okv_stage(okv_ctx* c, int32_t layer, const void* draft_q, int32_t step, float fetch_cap,
                      void* stream) {
   if (!c) return OKV_EINVAL;
-  return stage_impl(c, layer, draft_q, false, step, fetch_cap, stream);
+  return stage_impl(c, layer, draft_q, nullptr, step, fetch_cap, stream);
 }
 
 namespace {
@@ -848,10 +852,15 @@ okv_status okv_predict(okv_ctx* c, int32_t layer, const void* query, int32_t* co
   const LayerState S = layer_state(c, layer);
   const ReqTables T = req_tables(c);
   {
+    Timer t(c, OKV_K_COEF, ss);
+    OKV_CUDA(c, okv::launch_coef(G, c->active_dev, n_active, 1, query, 0, c->pred_coef, 0, ss));
+    t.stop(1);
+  }
+  {
     Timer t(c, OKV_K_SCORE_TOPK, ss);
     int n = 0;
-    OKV_CUDA(c, okv::launch_stage(G, S, T, n_active, max_blocks_at(c, layer), query, c->scores, c->stage_arrivals,
-                                  1, 0, c->ctr_dev, c->err_dev, ss, &n, ids, counts));
+    OKV_CUDA(c, okv::launch_stage(G, S, T, n_active, max_blocks_at(c, layer), c->pred_coef, c->scores,
+                                  c->stage_arrivals, 1, 0, c->ctr_dev, c->err_dev, ss, &n, ids, counts));
     t.stop(n);
   }
   if (!c->stage_on_caller) {
@@ -880,21 +889,24 @@ okv_status okv_step(okv_ctx* c, const void* q, const void* draft_q, void* out, c
   const size_t qbytes = (size_t)G.R * G.Hq * G.d * G.elem;
   const size_t kvbytes = (size_t)G.R * G.Hkv * G.d * G.elem;
   cudaStream_t s = (cudaStream_t)stream;
-  // One copy of every layer's draft, into the half of step_drafts the step before last used
-  // (its stagings have read it long since), instead of one copy per layer on the caller's stream.
+  // The scoring coefficients of every layer's draft in one launch, into the half of step_coef
+  // the step before last used (its stagings have read it long since), instead of one launch per
+  // layer on the caller's stream; the caller may then reuse draft_q.
   const int p = c->step_parity;
-  const uint8_t* drafts = (const uint8_t*)draft_q;
-  const bool copied = !c->stage_on_caller;
-  if (copied) {
-    uint8_t* dst = c->step_drafts + (size_t)p * G.L * qbytes;
-    if (c->step_used[p]) {
-      OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_step_read[p], 0));
-      if (c->sel_stream2) OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_step_read2[p], 0));
-    }
-    OKV_CUDA(c, cudaMemcpyAsync(dst, draft_q, (size_t)G.L * qbytes, cudaMemcpyDeviceToDevice, s));
-    drafts = dst;
-    c->step_parity ^= 1;
+  const size_t cstride = (size_t)c->per_layer_units * 2 * G.d;  // floats of one layer
+  float* coefs = c->step_coef + (size_t)p * G.L * cstride;
+  if (c->step_used[p]) {
+    OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_step_read[p], 0));
+    if (c->sel_stream2) OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_step_read2[p], 0));
   }
+  {
+    Timer t(c, OKV_K_COEF, s);
+    OKV_CUDA(c, okv::launch_coef(G, c->active_dev, (int32_t)c->active_list.size(), G.L, draft_q,
+                                 (int64_t)G.R * G.Hq * G.d, coefs, (int64_t)cstride, s));
+    t.stop(c->active_list.empty() ? 0 : 1);
+  }
+  c->step_parity ^= 1;
+  const uint8_t* drafts = (const uint8_t*)draft_q;
   if (k_new) {
     // Every layer's append goes on the append stream at once, each after its layer's last
     // staging; the caller's stream waits for a layer's append only before that layer's attention.
@@ -913,14 +925,12 @@ okv_status okv_step(okv_ctx* c, const void* q, const void* draft_q, void* out, c
     if (k_new) OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_appended[l], 0));
     okv_status st = okv_attend(c, l, (const uint8_t*)q + l * qbytes, (uint8_t*)out + l * qbytes, stream);
     if (st != OKV_OK) return st;
-    st = stage_impl(c, l, drafts + l * qbytes, copied, step, fetch_cap, stream);
+    st = stage_impl(c, l, drafts + l * qbytes, coefs + (size_t)l * cstride, step, fetch_cap, stream);
     if (st != OKV_OK) return st;
   }
-  if (copied) {
-    OKV_CUDA(c, cudaEventRecord(c->ev_step_read[p], c->sel_stream));
-    if (c->sel_stream2) OKV_CUDA(c, cudaEventRecord(c->ev_step_read2[p], c->sel_stream2));
-    c->step_used[p] = true;
-  }
+  OKV_CUDA(c, cudaEventRecord(c->ev_step_read[p], c->sel_stream));
+  if (c->sel_stream2) OKV_CUDA(c, cudaEventRecord(c->ev_step_read2[p], c->sel_stream2));
+  c->step_used[p] = true;
   return OKV_OK;
 }
 

@@ -99,8 +99,13 @@ cudaError_t launch_reset_request(const Geom& G, const StateBase& B, const Reques
 // Dynamic shared memory of one staging CTA for contexts of up to nb_cap blocks: the selection
 // keeps per-block arrays of the unit (score images, block -> slot map, candidates) on chip.
 size_t stage_smem_bytes(const Geom& G, int32_t nb_cap);
+// The scoring's coefficients of `layers` layers of draft queries (layer l at draft +
+// l * draft_layer_stride elements, [R][Hq][d] storage) into coef (layer l at coef +
+// l * coef_layer_stride floats, [R][Hkv][2d]: N then P), for the active requests.
+cudaError_t launch_coef(const Geom& G, const int32_t* active, int32_t n_active, int32_t layers, const void* draft,
+                        int64_t draft_layer_stride, float* coef, int64_t coef_layer_stride, cudaStream_t s);
 cudaError_t launch_stage(const Geom& G, const LayerState& S, const ReqTables& T, int32_t n_active,
-                         int32_t max_nb, const void* draft, uint32_t* scores, int32_t* arrivals,
+                         int32_t max_nb, const float* coef, uint32_t* scores, int32_t* arrivals,
                          int32_t cap_blocks, int32_t step, Counters* ctr, int32_t* err, cudaStream_t s,
                          int* n_launches, int32_t* pred_ids = nullptr, int32_t* pred_n = nullptr);
 // `work`: two int32 counters of this layer that start at zero and are left at zero.
