@@ -338,3 +338,39 @@ def test_step_with_appends_every_unit():
             assert rig.ctx.read_lengths(l)[:3].tolist() == [1020, 2060, 3020]
     finally:
         rig.close()
+
+
+@pytest.mark.parametrize("env", [{"OKV_STAGE_LANES": "1"}, {"OKV_STAGE_LANES": "2"},
+                                 {"OKV_STAGE_STREAM": "caller"}, {"OKV_STAGE_PRIORITY": "high"}])
+def test_staging_stream_layouts(env, monkeypatch):
+    """The staging's stream layouts (read at okv_create): one or two staging lanes (odd layers on
+    the second), staging on the caller's stream, staging at the greatest priority; okv_stage and
+    okv_step over 3 layers, bootstrap and 3 capped steps, every unit checked after every step."""
+    import torch
+    import oracle as O
+    from okv_harness import to_device, torch_dtype
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    w = QWEN.scaled(layers=3, batch=3, context=4096)
+    rig = Rig(w)
+    try:
+        L, R, Hq, d = w.layers, rig.R, w.q_heads, w.head_dim
+        C = O.fetch_cap_blocks(w.fetch_cap, rig.kb)
+        for l in range(L):  # okv_stage, one layer at a time
+            rig.stage(l, 0, 1.0, draft_step=-1)
+        for t in range(3):  # okv_step, every layer
+            q = np.stack([rig.batch_queries(l, t, 0) for l in range(L)])
+            dr = np.stack([rig.batch_queries(l, t, 1) for l in range(L)])
+            out = torch.zeros((L, R, Hq, d), dtype=torch_dtype(w.dtype), device="cuda")
+            rig.ctx.step(to_device(q, w.dtype), to_device(dr, w.dtype), out, t + 1)
+            torch.cuda.synchronize()
+            assert rig.ctx.sync(60_000) == 0
+            for l in range(L):
+                assert rig.check_attention(l, q[l], out[l]) <= ATOL[BF16]
+                rig.model.score_topk(l, dr[l])
+                gsel, _ = rig.check_selection(l)
+                rig.model.select(l, C, t + 1, sel_override=gsel)
+                rig.check_tables(l)
+                rig.check_pool(l)
+    finally:
+        rig.close()
