@@ -94,6 +94,7 @@ struct okv_ctx {
   // streams and events
   cudaStream_t sel_stream = nullptr, copy_stream = nullptr;
   cudaStream_t sel_stream2 = nullptr;        // the second staging lane, or NULL
+  cudaStream_t att_stream = nullptr;         // okv_step's attentions at the greatest priority, or NULL
   cudaStream_t app_stream = nullptr;         // okv_step's appends, ahead of the caller's stream
   std::vector<cudaEvent_t> ev_appended;      // [layers]: the last append of each layer
   cudaEvent_t ev_in = nullptr;
@@ -291,6 +292,7 @@ void okv_destroy(okv_ctx* c) {
   if (!c) return;
   if (c->sel_stream) cudaStreamSynchronize(c->sel_stream);
   if (c->sel_stream2) cudaStreamSynchronize(c->sel_stream2);
+  if (c->att_stream) cudaStreamSynchronize(c->att_stream);
   if (c->copy_stream) cudaStreamSynchronize(c->copy_stream);
   if (c->app_stream) cudaStreamSynchronize(c->app_stream);
   for (auto& t : c->pending) {
@@ -306,6 +308,7 @@ void okv_destroy(okv_ctx* c) {
   for (auto e : c->ev_step_read2) if (e) cudaEventDestroy(e);
   if (c->sel_stream) cudaStreamDestroy(c->sel_stream);
   if (c->sel_stream2) cudaStreamDestroy(c->sel_stream2);
+  if (c->att_stream) cudaStreamDestroy(c->att_stream);
   if (c->copy_stream) cudaStreamDestroy(c->copy_stream);
   if (c->app_stream) cudaStreamDestroy(c->app_stream);
   void* bufs[] = {c->summ, c->pool, c->slot_block, c->stamp, c->sel_ids, c->sel_scores,
@@ -469,6 +472,10 @@ okv_status okv_create(const okv_config* cfg, okv_ctx** out) {
   c->stage_on_caller = ps && strcmp(ps, "caller") == 0;
   ck(cudaStreamCreateWithPriority(&c->sel_stream, cudaStreamNonBlocking, prio));
   if (c->scores2) ck(cudaStreamCreateWithPriority(&c->sel_stream2, cudaStreamNonBlocking, prio));
+  // OKV_ATTEND_PRIORITY=high: okv_step runs its attentions on an internal stream of the greatest
+  // priority (joined back to the caller's stream at the end of the step)
+  const char* pa = getenv("OKV_ATTEND_PRIORITY");
+  if (pa && strcmp(pa, "high") == 0) ck(cudaStreamCreateWithPriority(&c->att_stream, cudaStreamNonBlocking, hi));
   ck(cudaStreamCreateWithPriority(&c->copy_stream, cudaStreamNonBlocking, hi));
   ck(cudaStreamCreateWithPriority(&c->app_stream, cudaStreamNonBlocking, hi));
   ck(cudaEventCreateWithFlags(&c->ev_in, cudaEventDisableTiming));
@@ -892,17 +899,26 @@ okv_status okv_step(okv_ctx* c, const void* q, const void* draft_q, void* out, c
   // The scoring coefficients of every layer's draft in one launch, into the half of step_coef
   // the step before last used (its stagings have read it long since), instead of one launch per
   // layer on the caller's stream; the caller may then reuse draft_q.
+  // The step's own work (coefficients, attentions, the staging's waits on them) runs on the
+  // caller's stream, or on the internal high-priority stream, which first takes up the caller's
+  // work so far and which the caller's stream waits for at the end.
+  cudaStream_t as = s;
+  if (c->att_stream) {
+    OKV_CUDA(c, cudaEventRecord(c->ev_in, s));
+    OKV_CUDA(c, cudaStreamWaitEvent(c->att_stream, c->ev_in, 0));
+    as = c->att_stream;
+  }
   const int p = c->step_parity;
   const size_t cstride = (size_t)c->per_layer_units * 2 * G.d;  // floats of one layer
   float* coefs = c->step_coef + (size_t)p * G.L * cstride;
   if (c->step_used[p]) {
-    OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_step_read[p], 0));
-    if (c->sel_stream2) OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_step_read2[p], 0));
+    OKV_CUDA(c, cudaStreamWaitEvent(as, c->ev_step_read[p], 0));
+    if (c->sel_stream2) OKV_CUDA(c, cudaStreamWaitEvent(as, c->ev_step_read2[p], 0));
   }
   {
-    Timer t(c, OKV_K_COEF, s);
+    Timer t(c, OKV_K_COEF, as);
     OKV_CUDA(c, okv::launch_coef(G, c->active_dev, (int32_t)c->active_list.size(), G.L, draft_q,
-                                 (int64_t)G.R * G.Hq * G.d, coefs, (int64_t)cstride, s));
+                                 (int64_t)G.R * G.Hq * G.d, coefs, (int64_t)cstride, as));
     t.stop(c->active_list.empty() ? 0 : 1);
   }
   c->step_parity ^= 1;
@@ -912,7 +928,7 @@ okv_status okv_step(okv_ctx* c, const void* q, const void* draft_q, void* out, c
     // staging; the caller's stream waits for a layer's append only before that layer's attention.
     for (int32_t l = 0; l < G.L; ++l)
       if (okv_status st = append_check(c, l)) return st;
-    OKV_CUDA(c, cudaEventRecord(c->ev_in, s));  // k_new / v_new are ready
+    OKV_CUDA(c, cudaEventRecord(c->ev_in, as));  // k_new / v_new are ready
     OKV_CUDA(c, cudaStreamWaitEvent(c->app_stream, c->ev_in, 0));
     for (int32_t l = 0; l < G.L; ++l) {
       okv_status st = append_enqueue(c, l, (const uint8_t*)k_new + l * kvbytes, (const uint8_t*)v_new + l * kvbytes,
@@ -922,11 +938,15 @@ okv_status okv_step(okv_ctx* c, const void* q, const void* draft_q, void* out, c
     }
   }
   for (int32_t l = 0; l < G.L; ++l) {
-    if (k_new) OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_appended[l], 0));
-    okv_status st = okv_attend(c, l, (const uint8_t*)q + l * qbytes, (uint8_t*)out + l * qbytes, stream);
+    if (k_new) OKV_CUDA(c, cudaStreamWaitEvent(as, c->ev_appended[l], 0));
+    okv_status st = okv_attend(c, l, (const uint8_t*)q + l * qbytes, (uint8_t*)out + l * qbytes, as);
     if (st != OKV_OK) return st;
-    st = stage_impl(c, l, drafts + l * qbytes, coefs + (size_t)l * cstride, step, fetch_cap, stream);
+    st = stage_impl(c, l, drafts + l * qbytes, coefs + (size_t)l * cstride, step, fetch_cap, as);
     if (st != OKV_OK) return st;
+  }
+  if (c->att_stream) {
+    OKV_CUDA(c, cudaEventRecord(c->ev_in, as));
+    OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_in, 0));
   }
   OKV_CUDA(c, cudaEventRecord(c->ev_step_read[p], c->sel_stream));
   if (c->sel_stream2) OKV_CUDA(c, cudaEventRecord(c->ev_step_read2[p], c->sel_stream2));
@@ -945,6 +965,10 @@ okv_status okv_join(okv_ctx* c, void* stream) {
     OKV_CUDA(c, cudaEventRecord(c->ev_in, c->sel_stream2));
     OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_in, 0));
   }
+  if (c->att_stream) {
+    OKV_CUDA(c, cudaEventRecord(c->ev_in, c->att_stream));
+    OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_in, 0));
+  }
   OKV_CUDA(c, cudaEventRecord(c->ev_in, c->copy_stream));
   OKV_CUDA(c, cudaStreamWaitEvent(s, c->ev_in, 0));
   return OKV_OK;
@@ -953,9 +977,11 @@ okv_status okv_join(okv_ctx* c, void* stream) {
 okv_status okv_sync(okv_ctx* c, int64_t timeout_ms) {
   if (!c) return OKV_EINVAL;
   // one event at the end of each internal stream (staging, gather, appends of okv_step)
-  cudaStream_t streams[4] = {c->sel_stream, c->copy_stream, c->app_stream, c->sel_stream2};
-  const int ns = c->sel_stream2 ? 4 : 3;
-  cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
+  cudaStream_t streams[5] = {c->sel_stream, c->copy_stream, c->app_stream, nullptr, nullptr};
+  int ns = 3;
+  if (c->sel_stream2) streams[ns++] = c->sel_stream2;
+  if (c->att_stream) streams[ns++] = c->att_stream;
+  cudaEvent_t ev[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
   for (int i = 0; i < ns; ++i) {
     OKV_CUDA(c, cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming));
     OKV_CUDA(c, cudaEventRecord(ev[i], streams[i]));
