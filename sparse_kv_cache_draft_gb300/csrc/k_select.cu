@@ -500,7 +500,7 @@ stage_kernel(Geom G, LayerState S, ReqTables RT, int32_t chunks, int32_t nb_cap,
   const int32_t ua = blockIdx.x / chunks, chunk = blockIdx.x % chunks;
   const int32_t a = ua / G.Hkv, h = ua % G.Hkv;
   const int32_t r = RT.active[a];
-  const int32_t len = S.len[r];
+  const int32_t len = S.len_act[a];  // (not S.len[r]: no wait for r first)
   const int32_t nb = (len + G.bs - 1) / G.bs;
   const int32_t b_lo = chunk * kScoreChunk;
   const bool bad = len < 0 || nb > G.nb_max || nb > nb_cap;

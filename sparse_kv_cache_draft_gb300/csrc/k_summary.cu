@@ -151,6 +151,7 @@ __global__ void append_kernel(Geom G, LayerState S, ReqTables T_, int32_t layer,
     arrivals[r] = 0;
     __threadfence();
     S.len[r] = pos + 1;
+    S.len_act[blockIdx.x] = pos + 1;
   }
 }
 

@@ -50,6 +50,7 @@ struct okv_ctx {
   int32_t* fetch = nullptr;
   int32_t* n_fetch = nullptr;
   int32_t* len = nullptr;
+  int32_t* len_active = nullptr;   // [layers][R]: the lengths by position in the active list
   int32_t* active_dev = nullptr;
   uint64_t* host_kv_dev = nullptr;
   int32_t* cap_dev = nullptr;
@@ -150,6 +151,7 @@ LayerState layer_state(const okv_ctx* c, int32_t layer) {
   S.fetch = c->fetch + layer * U * G.kb * 2;
   S.n_fetch = c->n_fetch + layer * U;
   S.len = c->len + (int64_t)layer * G.R;
+  S.len_act = c->len_active + (int64_t)layer * G.R;
   S.local_of = c->local_of + layer * U * G.nb_max;
   S.local_used = c->local_used + layer * U;
   S.route = c->route + layer * U * G.kb;
@@ -224,6 +226,7 @@ okv_status sync_internal(okv_ctx* c) {
   OKV_CUDA(c, cudaStreamSynchronize(c->app_stream));
   OKV_CUDA(c, cudaStreamSynchronize(c->sel_stream));
   if (c->sel_stream2) OKV_CUDA(c, cudaStreamSynchronize(c->sel_stream2));
+  if (c->att_stream) OKV_CUDA(c, cudaStreamSynchronize(c->att_stream));
   OKV_CUDA(c, cudaStreamSynchronize(c->copy_stream));
   return OKV_OK;
 }
@@ -232,9 +235,17 @@ okv_status upload_active(okv_ctx* c) {
   c->active_list.clear();
   for (int32_t r = 0; r < c->G.R; ++r)
     if (c->active[r]) c->active_list.push_back(r);
-  if (!c->active_list.empty())
+  if (!c->active_list.empty()) {
     OKV_CUDA(c, cudaMemcpy(c->active_dev, c->active_list.data(), c->active_list.size() * sizeof(int32_t),
                            cudaMemcpyHostToDevice));
+    // the lengths by active position (the staging reads a unit's length without first reading its
+    // request id; the append kernel keeps both copies advancing together)
+    std::vector<int32_t> la((size_t)c->G.L * c->G.R, 0);
+    for (int32_t l = 0; l < c->G.L; ++l)
+      for (size_t a = 0; a < c->active_list.size(); ++a)
+        la[(size_t)l * c->G.R + a] = c->len_host[(size_t)l * c->G.R + c->active_list[a]];
+    OKV_CUDA(c, cudaMemcpy(c->len_active, la.data(), la.size() * sizeof(int32_t), cudaMemcpyHostToDevice));
+  }
   // shared host buffers among active requests
   for (int32_t r = 0; r < c->G.R; ++r) c->shared_buf[r] = 0;
   for (size_t i = 0; i < c->active_list.size(); ++i)
@@ -312,7 +323,7 @@ void okv_destroy(okv_ctx* c) {
   if (c->copy_stream) cudaStreamDestroy(c->copy_stream);
   if (c->app_stream) cudaStreamDestroy(c->app_stream);
   void* bufs[] = {c->summ, c->pool, c->slot_block, c->stamp, c->sel_ids, c->sel_scores,
-                  c->n_sel, c->fetch, c->n_fetch, c->len, c->active_dev, c->host_kv_dev, c->cap_dev,
+                  c->n_sel, c->fetch, c->n_fetch, c->len, c->len_active, c->active_dev, c->host_kv_dev, c->cap_dev,
                   c->err_dev, c->ctr_dev, c->partials, c->coef_buf, c->pred_coef, c->scores, c->stage_arrivals, c->attend_arrivals,
                   c->scores2, c->stage_arrivals2,
                   c->local_of, c->local_used, c->route, c->local_kv_dev, c->local_cap_dev,
@@ -398,6 +409,7 @@ okv_status okv_create(const okv_config* cfg, okv_ctx** out) {
             alloc((void**)&c->sel_ids, L * U * G.kb * 4) && alloc((void**)&c->sel_scores, L * U * G.kb * 4) &&
             alloc((void**)&c->n_sel, L * U * 4) && alloc((void**)&c->fetch, L * U * G.kb * 8) &&
             alloc((void**)&c->n_fetch, L * U * 4) && alloc((void**)&c->len, L * G.R * 4) &&
+            alloc((void**)&c->len_active, L * G.R * 4) &&
             alloc((void**)&c->active_dev, G.R * 4) && alloc((void**)&c->host_kv_dev, G.R * 8) &&
             alloc((void**)&c->cap_dev, G.R * 4) && alloc((void**)&c->err_dev, 16) &&
             alloc((void**)&c->ctr_dev, sizeof(Counters)) &&
@@ -440,6 +452,7 @@ okv_status okv_create(const okv_config* cfg, okv_ctx** out) {
   ck(cudaMemset(c->n_sel, 0, L * U * 4));
   ck(cudaMemset(c->n_fetch, 0, L * U * 4));
   ck(cudaMemset(c->len, 0, L * G.R * 4));
+  ck(cudaMemset(c->len_active, 0, L * G.R * 4));
   ck(cudaMemset(c->err_dev, 0, 16));
   ck(cudaMemset(c->stage_arrivals, 0, U * 4));
   if (c->stage_arrivals2) ck(cudaMemset(c->stage_arrivals2, 0, U * 4));

@@ -43,6 +43,7 @@ struct LayerState {
   int32_t* fetch;       // [R][Hkv][kb][2] (block, slot)
   int32_t* n_fetch;     // [R][Hkv]
   int32_t* len;         // [R] tokens of each request at this layer
+  int32_t* len_act;     // [n_active] the same, indexed by position in the active list
   // decode-side tier of partially staged requests
   int32_t* local_of;    // [R][Hkv][nb_max] block -> kept entry or -1
   int32_t* local_used;  // [R][Hkv] entries in use
