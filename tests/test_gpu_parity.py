@@ -376,3 +376,27 @@ def test_staging_stream_layouts(env, monkeypatch):
                 rig.check_pool(l)
     finally:
         rig.close()
+
+
+def test_bytes_moved_equal_the_fetch_lists():
+    """The gather's count of blocks moved host -> HBM (okv_timing.fetched_blocks, a device counter)
+    equals the blocks of the oracle's fetch lists over a bootstrap and 4 capped steps, so the bytes
+    per step the benchmark reports are the fetch lists' blocks times 8 KiB."""
+    w = QWEN.scaled(layers=2, batch=3)
+    rig = Rig(w)
+    try:
+        rig.ctx.set_timing(True)
+        want = 0
+        for layer in range(2):
+            rig.stage(layer, 0, 1.0, draft_step=-1)
+            want += int(rig.model.n_fetch[layer].sum())
+        for t in range(4):
+            for layer in range(2):
+                rig.attend(layer, t)
+                rig.stage(layer, t + 1, 0.05, draft_step=t)
+                want += int(rig.model.n_fetch[layer].sum())
+        got = rig.ctx.read_timing()["fetched_blocks"]
+        assert got == want, (got, want)
+        assert want > 2 * 3 * 8 * 128  # the bootstrap filled every pool, then capped steps added more
+    finally:
+        rig.close()
