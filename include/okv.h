@@ -73,9 +73,12 @@ typedef struct okv_ctx okv_ctx;
 
 /* Create a context on the current CUDA device. Allocates in HBM: block summaries
  * [layers][max_requests][kv_heads][max_blocks][2][head_dim], the slot pool
- * [layers][max_requests][kv_heads][Kb][2][block_size][head_dim], the per-unit tables and the
- * device error word; creates two internal streams. EINVAL on an unsupported config, ENOMEM
- * if HBM is short. */
+ * [layers][max_requests][kv_heads][Kb][2][block_size][head_dim], the per-unit tables, the
+ * scoring coefficients and the device error word; creates its internal streams (two staging
+ * lanes at the least priority, the gather's copy stream and okv_step's append stream at the
+ * greatest). Environment variables read here select measured alternatives: OKV_STAGE_LANES=1,
+ * OKV_STAGE_STREAM=caller, OKV_STAGE_PRIORITY=high, OKV_ATTEND_PRIORITY=high. EINVAL on an
+ * unsupported config, ENOMEM if HBM is short. */
 OKV_API okv_status okv_create(const okv_config* cfg, okv_ctx** out);
 /* Waits for the context's work, frees everything it allocated. NULL is a no-op. */
 OKV_API void okv_destroy(okv_ctx* ctx);
