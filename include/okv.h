@@ -257,7 +257,7 @@ OKV_API int64_t okv_launch_count(const okv_ctx* ctx);
  *
  * Some callers cannot call cudaMalloc: code that runs where allocation is forbidden or must
  * not fail (a fixed memory budget handed over up front, an allocator they do not own, a
- * graph or callback path that may not allocate). okv_attend_static gives them the sparse
+ * callback path that may not allocate). okv_attend_static gives them the sparse
  * attention of okv_attend without a context and without allocating anything: the caller
  * passes every input and output, and the kernels' only workspace (split partials, request ids,
  * an error word) is one fixed 16 MiB device array inside this library, which every GPU that
@@ -277,7 +277,7 @@ OKV_API int64_t okv_launch_count(const okv_ctx* ctx);
  * Every call resolves the array's device address on the current device
  * (cudaGetSymbolAddress). The first call in each CUDA context of a device (the first call on
  * the device, and the first after a cudaDeviceReset) also initialises the array's constant
- * part, synchronising that device: make it before any stream capture. Calls then enqueue on
+ * part, synchronising that device. Calls then enqueue on
  * `stream`, which must belong to the current device (else OKV_EINVAL): two small clears of
  * the array (split counters, error word), then the attention kernels. All calls share the
  * array: calls whose work overlaps on the GPU (on different streams, or on different host
