@@ -75,10 +75,11 @@ typedef struct okv_ctx okv_ctx;
  * [layers][max_requests][kv_heads][max_blocks][2][head_dim], the slot pool
  * [layers][max_requests][kv_heads][Kb][2][block_size][head_dim], the per-unit tables, the
  * scoring coefficients and the device error word; creates its internal streams (two staging
- * lanes at the least priority, the gather's copy stream and okv_step's append stream at the
- * greatest). Environment variables read here select measured alternatives: OKV_STAGE_LANES=1,
- * OKV_STAGE_STREAM=caller, OKV_STAGE_PRIORITY=high, OKV_ATTEND_PRIORITY=high. EINVAL on an
- * unsupported config, ENOMEM if HBM is short. */
+ * lanes at the least priority, okv_step's attention stream at a middle priority, the gather's
+ * copy stream and okv_step's append stream at the greatest). Environment variables read here
+ * select measured alternatives: OKV_STAGE_LANES=1, OKV_STAGE_STREAM=caller,
+ * OKV_STAGE_PRIORITY=high, OKV_ATTEND_PRIORITY=caller or high. EINVAL on an unsupported config,
+ * ENOMEM if HBM is short. */
 OKV_API okv_status okv_create(const okv_config* cfg, okv_ctx** out);
 /* Waits for the context's work, frees everything it allocated. NULL is a no-op. */
 OKV_API void okv_destroy(okv_ctx* ctx);
@@ -179,11 +180,13 @@ OKV_API okv_status okv_attend_lookahead(okv_ctx* ctx, int32_t layer, const void*
  * later layers). The result is that of: for l = 0 .. layers-1: okv_append(l) if k_new is not NULL,
  * okv_attend(l), okv_stage(l, step). q, draft_q, out: device [layers][max_requests][q_heads]
  * [head_dim]; k_new, v_new: device [layers][max_requests][kv_heads][head_dim] or NULL.
- * Scheduling: the scoring coefficients of every layer's draft are computed in one launch, up
- * front, on `stream`. Every layer's append is enqueued
- * up front on an internal stream, each after that layer's previous staging. On `stream`, the
- * attention of layer l waits only for the append of layer l. The inputs may be reused by work
- * enqueued on `stream` after the call. Stops at the first failing check (before any work is
+ * Scheduling: the step's own work runs on the context's attention stream, which first waits
+ * for the work enqueued on `stream` so far and which `stream` waits for at the end of the step
+ * (with OKV_ATTEND_PRIORITY=caller, on `stream` itself). There the scoring coefficients of every
+ * layer's draft are computed in one launch, up front, then the attentions run in layer order,
+ * the attention of layer l waiting only for the append of layer l. Every layer's append is
+ * enqueued up front on an internal stream, each after that layer's previous staging. The
+ * inputs may be reused by work enqueued on `stream` after the call. Stops at the first failing check (before any work is
  * enqueued, for the append checks) and returns its status. */
 OKV_API okv_status okv_step(okv_ctx* ctx, const void* q, const void* draft_q, void* out,
                             const void* k_new, const void* v_new, int32_t step, float fetch_cap,

@@ -95,7 +95,7 @@ struct okv_ctx {
   // streams and events
   cudaStream_t sel_stream = nullptr, copy_stream = nullptr;
   cudaStream_t sel_stream2 = nullptr;        // the second staging lane, or NULL
-  cudaStream_t att_stream = nullptr;         // okv_step's attentions at the greatest priority, or NULL
+  cudaStream_t att_stream = nullptr;         // okv_step's coefficients and attentions, or NULL: the caller's stream
   cudaStream_t app_stream = nullptr;         // okv_step's appends, ahead of the caller's stream
   std::vector<cudaEvent_t> ev_appended;      // [layers]: the last append of each layer
   cudaEvent_t ev_in = nullptr;
@@ -469,26 +469,33 @@ okv_status okv_create(const okv_config* cfg, okv_ctx** out) {
   ck(cudaMemset(c->gather_work, 0, (size_t)L * 2 * 4));
   int lo = 0, hi = 0;
   ck(cudaDeviceGetStreamPriorityRange(&lo, &hi));
-  // Scoring and selection run on the internal select stream at the least priority, which is
-  // also the priority of the default streams a caller's attention usually runs on: the two
-  // HBM-bound kernels share the SMs as equals. (Measured on GB300, 16K / b128: 10.2K tok/s
-  // against 9.4K with scoring on the caller's stream after the attention and 8.2K with staging
-  // at the greatest priority; running okv_step's attentions on a
-  // stream above the staging raised the attention's in-step share of the HBM peak from 0.64 to
-  // 0.73 but cost 4% of tok/s, the staging then falling behind the gather.) The gather runs on
-  // the copy stream at the greatest priority: the host link is the longest pole of a step, so
-  // the gather must never wait for SMs. OKV_STAGE_STREAM=caller and OKV_STAGE_PRIORITY=high
-  // select the alternatives.
+  // Three priority levels. Scoring and selection run on the internal select streams at the least
+  // priority. The gather (copy stream) and okv_step's appends run at the greatest: the host link
+  // is the longest pole of a step, so the gather must never wait for SMs. okv_step's own work
+  // (the coefficients of every layer, then the attentions) runs on an internal stream between
+  // the two, joined back to the caller's stream at the end of the step: the attention of a layer
+  // then takes SMs before the background staging but after the gather. Measured on GB300
+  // (interleaved pairs, median of three timed regions each):
+  //   - 16K / b128: the same tok/s (12.37K against 12.43K median over four pairs), e2e higher in
+  //     every pair (+1.4% to +8.2%), the attention's in-step share of the HBM peak 0.73-0.76
+  //     against 0.56-0.58 on the caller's stream;
+  //   - 32K / b32: +1.6% to +9.3% tok/s in three of three pairs;
+  //   - at the greatest priority, beside the gather: the same tok/s but e2e 15-20% lower.
+  // Alternatives: OKV_ATTEND_PRIORITY=caller (okv_step's work on the caller's stream),
+  // OKV_ATTEND_PRIORITY=high (the greatest priority), OKV_STAGE_STREAM=caller (staging on the
+  // caller's stream after the attention: 9.4K against 10.2K tok/s in an earlier build),
+  // OKV_STAGE_PRIORITY=high (staging at the greatest priority: 8.2K).
   const char* pe = getenv("OKV_STAGE_PRIORITY");
   const int prio = (pe && strcmp(pe, "high") == 0) ? hi : lo;  // of the select stream
   const char* ps = getenv("OKV_STAGE_STREAM");
   c->stage_on_caller = ps && strcmp(ps, "caller") == 0;
   ck(cudaStreamCreateWithPriority(&c->sel_stream, cudaStreamNonBlocking, prio));
   if (c->scores2) ck(cudaStreamCreateWithPriority(&c->sel_stream2, cudaStreamNonBlocking, prio));
-  // OKV_ATTEND_PRIORITY=high: okv_step runs its attentions on an internal stream of the greatest
-  // priority (joined back to the caller's stream at the end of the step)
   const char* pa = getenv("OKV_ATTEND_PRIORITY");
-  if (pa && strcmp(pa, "high") == 0) ck(cudaStreamCreateWithPriority(&c->att_stream, cudaStreamNonBlocking, hi));
+  if (!(pa && strcmp(pa, "caller") == 0)) {
+    const int mid = (pa && strcmp(pa, "high") == 0) ? hi : (lo + hi) / 2;  // e.g. -2 in [-5, 0]
+    ck(cudaStreamCreateWithPriority(&c->att_stream, cudaStreamNonBlocking, mid));
+  }
   ck(cudaStreamCreateWithPriority(&c->copy_stream, cudaStreamNonBlocking, hi));
   ck(cudaStreamCreateWithPriority(&c->app_stream, cudaStreamNonBlocking, hi));
   ck(cudaEventCreateWithFlags(&c->ev_in, cudaEventDisableTiming));
@@ -913,8 +920,9 @@ okv_status okv_step(okv_ctx* c, const void* q, const void* draft_q, void* out, c
   // the step before last used (its stagings have read it long since), instead of one launch per
   // layer on the caller's stream; the caller may then reuse draft_q.
   // The step's own work (coefficients, attentions, the staging's waits on them) runs on the
-  // caller's stream, or on the internal high-priority stream, which first takes up the caller's
-  // work so far and which the caller's stream waits for at the end.
+  // internal attention stream (above the staging, below the gather), which first takes up the
+  // caller's work so far and which the caller's stream waits for at the end; with
+  // OKV_ATTEND_PRIORITY=caller it runs on the caller's stream itself.
   cudaStream_t as = s;
   if (c->att_stream) {
     OKV_CUDA(c, cudaEventRecord(c->ev_in, s));

@@ -342,12 +342,13 @@ def test_step_with_appends_every_unit():
 
 @pytest.mark.parametrize("env", [{"OKV_STAGE_LANES": "1"}, {"OKV_STAGE_LANES": "2"},
                                  {"OKV_STAGE_STREAM": "caller"}, {"OKV_STAGE_PRIORITY": "high"},
-                                 {"OKV_ATTEND_PRIORITY": "high"}])
+                                 {"OKV_ATTEND_PRIORITY": "high"}, {"OKV_ATTEND_PRIORITY": "caller"}])
 def test_staging_stream_layouts(env, monkeypatch):
-    """The staging's stream layouts (read at okv_create): one or two staging lanes (odd layers on
-    the second), staging on the caller's stream, staging at the greatest priority, okv_step's own
-    work at the greatest priority; okv_stage and okv_step over 3 layers, bootstrap and 3 capped
-    steps, every unit checked after every step."""
+    """The stream layouts (read at okv_create): one or two staging lanes (odd layers on the
+    second), staging on the caller's stream, staging at the greatest priority, okv_step's own work
+    at the greatest priority or on the caller's stream (instead of its attention stream at a
+    middle priority); okv_stage and okv_step over 3 layers, bootstrap and 3 capped steps, every
+    unit checked after every step."""
     import torch
     import oracle as O
     from okv_harness import to_device, torch_dtype
