@@ -86,6 +86,20 @@ def test_profiled_traffic_follows_the_kernel_sources(tmp_path, monkeypatch):
     assert bench.profiled_traffic("missing.md") is None
 
 
+def test_committed_traffic_lines_match_the_kernels():
+    """Every ncu traffic line committed under profiles/ names sources that still hash as recorded,
+    so the bench line carries the measured DRAM traffic of the kernels as they stand (a kernel
+    changed after its capture needs a new capture, or its line is stale and this fails)."""
+    import bench
+    lines = 0
+    for name in sorted(os.listdir(os.path.join(bench.ROOT, "profiles"))):
+        text = open(os.path.join(bench.ROOT, "profiles", name)).read()
+        if "bench: traffic_bytes_per_launch=" in text:
+            lines += 1
+            assert bench.profiled_traffic(name) is not None, name
+    assert lines >= 2  # the attention and the staging kernels
+
+
 def test_gpus_flag_launches_the_ranks():
     """`bench.py --gpus 2` with no torchrun environment starts two ranks (torchrun, 127.0.0.1); they
     join one process group and rank 0 alone prints the line (the reference arm on the CPU)."""
